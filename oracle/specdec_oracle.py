@@ -1,0 +1,398 @@
+"""CPU oracle for the per-round hot path of batch speculative decoding.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline /
+reference leg of ``bench.py`` may import this module.  The product path (the CUDA library and its
+Python binding) never imports, calls or links it, and it shares no code with that path: no helper,
+table or constant.  Inputs come from the seeded generators in
+``speculative_decoding_specdec_gb300.synth`` (which hold none of the method's arithmetic) or from
+hand-written fixtures.
+
+Everything here is plain numpy in float64, written for a reader to check against the pages by eye.
+Sources, cited by page title and section:
+
+* [IE5]   "Inference Engineering: Part 5/8: When Speculative Decoding Backfires"
+          - "Draft Possible Tokens, Then Verify Them Together"      (left-to-right acceptance, bonus)
+          - "One Verification Pass Can Commit Several Tokens"       (greedy worked example)
+          - "Exactness Means Different Things For Greedy And Sampled Output"
+                                                                     (min(1, p/q), normalize(max(0, p-q)))
+          - "Acceptance changes across the workload"                (discard after first rejection;
+                                                                     speculative KV commit/discard)
+* [BSDDR] "Batch Speculative Decoding Done Right" (technical summary of arXiv 2510.22876)
+          - section 2.1 (synchronisation invariants: rectangular alignment, position-ID contiguity)
+          - section 2.2 (EQSPEC unpad-append-repad)
+          - section 2.3 (EXSPEC SequencePool, grouping of same-length sequences)
+* [CF]    "Correctness Forensics for Batch Speculative Decoding: Diagnosing the Ragged Tensor
+          Problem", Abstract (ragged tensor problem, contiguous-layout realignment).
+
+Readings where the pages leave a step open (each is listed again in the design doc):
+
+* The target produces D+1 score rows per sequence; row j scores the token after the j-th draft
+  (row 0 after the last committed token).  The bonus needs the distribution "after the complete
+  draft" [IE5, Draft Possible Tokens], which is row D.
+* Greedy ties go to the lowest token index.  The pages are silent.
+* A draft x is accepted iff u < p(x)/q(x) with u uniform in [0, 1); this is the min(1, p/q) rule
+  with the min implicit.  u == p/q rejects.
+* Temperature T divides the scores of both models ("same sampling settings" [IE5, Exactness]).
+* The replacement or bonus token is an inverse-CDF draw with the row's last uniform u[b][D], over
+  token ids in ascending order, first k whose running sum exceeds u * (total).  If the residual
+  max(0, p - q) is all zero the draw falls back to p.
+* K/V state model: at round start row b holds N_b committed tokens right-aligned in width W; the
+  cache holds K/V for all of them but the last (the "pending" token, not yet run through the
+  target).  The verification pass writes K/V for [pending, d_1..d_D] at columns [W-1, W+D).
+  After acceptance a_b the surviving K/V columns are [W-N_b, W+a_b); the new pending token is the
+  replacement/bonus y_b.  The new width is W' = max_b (N_b + a_b + 1) (minimal padding).
+* Pad token ids are a caller-chosen ``pad_id``; pad position IDs are 0; pad K/V columns of the
+  destination are unspecified (left as they were).
+* Length grouping: within one length, rows in index order fill whole batches of ``bs`` first; the
+  remaining rows of every length, in (length, index) order, are chunked into mixed batches.
+  Uniform batches come first (ascending length), then mixed batches.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "OracleError",
+    "greedy_choice",
+    "verify_greedy",
+    "softmax",
+    "verify_sample",
+    "realign_plan",
+    "realign",
+    "check_invariants",
+    "group_by_length",
+    "pool_gather",
+    "pool_append",
+]
+
+
+class OracleError(ValueError):
+    """Raised for inputs the method does not define (the GPU path reports these as a status)."""
+
+
+# --------------------------------------------------------------------------------------------
+# Greedy verification  [IE5, "Exactness Means Different Things..." (greedy paragraph);
+#                       "Draft Possible Tokens, Then Verify Them Together"]
+# --------------------------------------------------------------------------------------------
+
+def greedy_choice(scores) -> int:
+    """The target's greedy choice for one score row: the highest score, lowest index on ties.
+
+    Greedy decoding "picks the token with the highest score" [IE5, opening section].  np.argmax
+    returns the first index of the maximum, which is the lowest-index tie rule.
+    """
+    row = np.asarray(scores, dtype=np.float64)
+    if np.isnan(row).any():
+        raise OracleError("NaN score")
+    return int(np.argmax(row))
+
+
+def verify_greedy(logits, draft):
+    """Greedy verification of a batch.
+
+    logits: [B, D+1, V] target scores; row j scores the token after draft j (row 0: after the
+            last committed token).
+    draft:  [B, D] draft token ids d_1..d_D.
+    Returns (accept_len[B], out_token[B]) as int32 arrays:
+      a_b = number of leading drafts equal to the target's choice (first mismatch stops the scan;
+            every later draft is discarded);
+      y_b = the target's choice at row a_b: the replacement for the rejected draft when a_b < D,
+            the bonus token when a_b == D.
+    """
+    logits = np.asarray(logits, dtype=np.float64)
+    draft = np.asarray(draft)
+    B, Dp1, V = logits.shape
+    D = Dp1 - 1
+    if draft.shape != (B, D):
+        raise OracleError("draft shape")
+    if ((draft < 0) | (draft >= V)).any():
+        raise OracleError("draft token out of range")
+    accept_len = np.zeros(B, dtype=np.int32)
+    out_token = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        choices = [greedy_choice(logits[b, j]) for j in range(D + 1)]
+        a = D
+        for j in range(D):               # read left to right, stop at the first rejection
+            if choices[j] != int(draft[b, j]):
+                a = j
+                break
+        accept_len[b] = a
+        out_token[b] = choices[a]        # replacement (a < D) or bonus (a == D)
+    return accept_len, out_token
+
+
+# --------------------------------------------------------------------------------------------
+# Sampled verification  [IE5, "Exactness Means Different Things For Greedy And Sampled Output"]
+# --------------------------------------------------------------------------------------------
+
+def softmax(scores, temperature: float):
+    """Probabilities of one score row at temperature T, in float64."""
+    x = np.asarray(scores, dtype=np.float64) / float(temperature)
+    e = np.exp(x - x.max())
+    return e / e.sum()
+
+
+def _inverse_cdf(weights, u: float):
+    """First k (ascending token id) whose running sum exceeds u * total; the running sum is
+    sequential.  If rounding leaves no such k, the last k with a nonzero weight."""
+    cdf = np.cumsum(weights)
+    total = cdf[-1]
+    t = u * total
+    k = int(np.searchsorted(cdf, t, side="right"))
+    if k >= len(weights):
+        k = int(np.nonzero(weights > 0)[0][-1])
+    lo = cdf[k - 1] if k > 0 else 0.0
+    return k, t, total, lo, cdf[k]
+
+
+def verify_sample(target_logits, draft_logits, draft, uniforms, temperature: float):
+    """Speculative rejection sampling over a batch.
+
+    target_logits: [B, D+1, V] scores of the main model (p after softmax at T).
+    draft_logits:  [B, D, V]   scores of the draft model (q after softmax at T).
+    draft:         [B, D]      the draft tokens (drawn from q by the draft model).
+    uniforms:      [B, D+1]    u[b][j], j < D decide the accept tests; u[b][D] drives the
+                               replacement/bonus draw.
+    For j = 0..D-1 (left to right): accept d_{j+1} iff u[b][j] < p_j(d)/q_j(d), i.e. with
+    probability min(1, p/q).  At the first rejection j*: draw y from normalize(max(0, p_j* - q_j*)).
+    If every draft is accepted: draw the bonus y from p_D.
+
+    Returns (accept_len[B], out_token[B], residual[B, V], trace) where residual[b] is the
+    normalised distribution y_b was drawn from, and trace holds float64 diagnostics for the
+    parity tolerance: ratio[B, D] (p/q of each evaluated test, NaN where not evaluated), and for
+    the draw t = u*R, R, and the running sums just below and at y.
+    """
+    tl = np.asarray(target_logits, dtype=np.float64)
+    dl = np.asarray(draft_logits, dtype=np.float64)
+    draft = np.asarray(draft)
+    u = np.asarray(uniforms, dtype=np.float64)
+    B, Dp1, V = tl.shape
+    D = Dp1 - 1
+    if dl.shape != (B, D, V) or draft.shape != (B, D) or u.shape != (B, D + 1):
+        raise OracleError("shape")
+    if not temperature > 0:
+        raise OracleError("temperature")
+    if ((draft < 0) | (draft >= V)).any():
+        raise OracleError("draft token out of range")
+    accept_len = np.zeros(B, dtype=np.int32)
+    out_token = np.zeros(B, dtype=np.int32)
+    residual = np.zeros((B, V), dtype=np.float64)
+    ratio = np.full((B, D), np.nan)
+    t_draw = np.zeros(B)
+    r_total = np.zeros(B)
+    cdf_lo = np.zeros(B)
+    cdf_hi = np.zeros(B)
+    for b in range(B):
+        a = D
+        for j in range(D):
+            p = softmax(tl[b, j], temperature)
+            q = softmax(dl[b, j], temperature)
+            x = int(draft[b, j])
+            r = p[x] / q[x] if q[x] > 0 else np.inf
+            ratio[b, j] = r
+            if not (u[b, j] < r):        # reject: stop here, later drafts are discarded
+                a = j
+                break
+        if a < D:
+            p = softmax(tl[b, a], temperature)
+            q = softmax(dl[b, a], temperature)
+            w = np.maximum(0.0, p - q)   # the probability still missing for each token
+            if not (w > 0).any():
+                w = p                    # unreachable unless p == q exactly
+        else:
+            w = softmax(tl[b, D], temperature)   # bonus: distribution after the full draft
+        k, t, total, lo, hi = _inverse_cdf(w, u[b, D])
+        accept_len[b] = a
+        out_token[b] = k
+        residual[b] = w / total
+        t_draw[b], r_total[b], cdf_lo[b], cdf_hi[b] = t, total, lo, hi
+    trace = {"ratio": ratio, "t": t_draw, "R": r_total, "cdf_lo": cdf_lo, "cdf_hi": cdf_hi}
+    return accept_len, out_token, residual, trace
+
+
+# --------------------------------------------------------------------------------------------
+# Realignment (EQSPEC unpad-append-repad)  [BSDDR 2.1, 2.2; CF Abstract; IE5 "Acceptance
+# changes across the workload" (commit accepted KV, discard speculative KV)]
+# --------------------------------------------------------------------------------------------
+
+def realign_plan(n_committed, width: int, accept_len, draft_len: int):
+    """Per-row column plan of one realignment.
+
+    Returns (n_new[B], W_new, src_lo[B], dst_lo[B], keep[B]):
+      N'_b  = N_b + a_b + 1                 (accepted drafts plus the replacement/bonus)
+      W'    = max_b N'_b                    (re-left-pad to the longest row)
+      keep_b = N'_b - 1 = N_b + a_b         (surviving K/V columns: committed, pending, accepted)
+      src_lo_b = W - N_b,  dst_lo_b = W' - N'_b
+    """
+    n = np.asarray(n_committed, dtype=np.int64)
+    a = np.asarray(accept_len, dtype=np.int64)
+    if (a < 0).any() or (a > draft_len).any():
+        raise OracleError("accept length out of range")
+    if (n < 1).any() or (n > width).any():
+        raise OracleError("committed length out of range")
+    n_new = n + a + 1
+    w_new = int(n_new.max()) if len(n_new) else 0
+    return n_new, w_new, width - n, w_new - n_new, n + a
+
+
+def realign(kv_src, kv_dst, n_committed, width: int, accept_len, out_token, draft, ids_src,
+            pad_id: int = 0):
+    """One EQSPEC realignment, out of place.
+
+    kv_src, kv_dst: [L, 2, B, H, S, hd] caches (any dtype; values are only moved).  kv_src holds
+                    K/V for columns [W-N_b, W+D) of row b (committed but pending, then the D+1
+                    columns the verification pass wrote).  kv_dst is the other buffer of the
+                    ping-pong pair; its pad columns are left as they were.
+    ids_src:        [B, S_src] token ids, row b's committed tokens at [W-N_b, W).
+    Returns (kv_out, ids[B, S_dst], mask[B, S_dst] uint8, pos[B, S_dst] int32, n_new[B], W').
+
+    Unpad each row, append the accepted drafts and the replacement/bonus token, re-left-pad to the
+    longest row, recompute position IDs from 0 over the content, and shift the surviving K/V
+    columns; the rejected drafts' columns [W+a_b, W+D) are discarded (never copied).
+    """
+    draft = np.asarray(draft)
+    B, D = draft.shape
+    S_src = kv_src.shape[4]
+    S_dst = kv_dst.shape[4]
+    if width + D > S_src:
+        raise OracleError("source capacity")
+    n_new, w_new, src_lo, dst_lo, keep = realign_plan(n_committed, width, accept_len, D)
+    if w_new + D > S_dst:
+        raise OracleError("capacity")   # the next verification pass could not be written
+    kv_out = np.array(kv_dst, copy=True)
+    ids = np.full((B, S_dst), pad_id, dtype=np.int32)
+    mask = np.zeros((B, S_dst), dtype=np.uint8)
+    pos = np.zeros((B, S_dst), dtype=np.int32)
+    n = np.asarray(n_committed, dtype=np.int64)
+    a = np.asarray(accept_len, dtype=np.int64)
+    for b in range(B):
+        s, d, k = int(src_lo[b]), int(dst_lo[b]), int(keep[b])
+        kv_out[:, :, b, :, d:d + k, :] = kv_src[:, :, b, :, s:s + k, :]
+        tokens = (list(np.asarray(ids_src[b, width - n[b]:width]))
+                  + list(draft[b, :a[b]]) + [int(out_token[b])])
+        ids[b, d:w_new] = tokens
+        mask[b, d:w_new] = 1
+        pos[b, d:w_new] = np.arange(n_new[b])
+    return kv_out, ids, mask, pos, n_new.astype(np.int32), w_new
+
+
+def check_invariants(mask, pos, n_committed, width: int):
+    """The two synchronisation invariants of [BSDDR 2.1] for a left-padded batch of width W.
+
+    (1) rectangular alignment: every row has pad + content == W (content right-aligned, ending
+        at column W-1, and nothing at or beyond W);
+    (2) position-ID contiguity: position IDs run 0, 1, ..., N_b-1 over the content columns that
+        the mask marks.
+    Returns a list of violation strings (empty when both hold).
+    """
+    bad = []
+    mask = np.asarray(mask)
+    pos = np.asarray(pos)
+    for b, nb in enumerate(np.asarray(n_committed)):
+        nb = int(nb)
+        row_m = mask[b]
+        content = np.nonzero(row_m)[0]
+        if len(content) != nb:
+            bad.append(f"row {b}: {len(content)} content columns, expected {nb}")
+            continue
+        if nb and (content[0] != width - nb or content[-1] != width - 1):
+            bad.append(f"row {b}: content not right-aligned at width {width}")
+        if (np.diff(content) != 1).any():
+            bad.append(f"row {b}: content not contiguous")
+        if (pos[b, content] != np.arange(nb)).any():
+            bad.append(f"row {b}: position IDs not 0..N-1 over content")
+    return bad
+
+
+# --------------------------------------------------------------------------------------------
+# EXSPEC grouping  [BSDDR 2.3: SequencePool, cross-batch grouping of same-length sequences]
+# --------------------------------------------------------------------------------------------
+
+def group_by_length(lengths, batch_size: int):
+    """Group pool rows into batches.
+
+    Rows of equal length, in index order, fill whole batches of ``batch_size`` (uniform batches:
+    no realignment needed).  What is left of every length, in (length, index) order, is cut into
+    mixed batches of at most ``batch_size`` rows (these are realigned).
+    Returns (perm[N], batch_offsets[nb+1], batch_uniform[nb], num_uniform).
+    """
+    lengths = [int(x) for x in lengths]
+    if batch_size < 1:
+        raise OracleError("batch size")
+    by_len = {}
+    for i in sorted(range(len(lengths)), key=lambda i: (lengths[i], i)):
+        by_len.setdefault(lengths[i], []).append(i)
+    batches, uniform, leftover = [], [], []
+    for length in sorted(by_len):
+        rows = by_len[length]
+        whole = len(rows) // batch_size * batch_size
+        for k in range(0, whole, batch_size):
+            batches.append(rows[k:k + batch_size])
+            uniform.append(1)
+        leftover.extend(rows[whole:])
+    num_uniform = len(batches)
+    for k in range(0, len(leftover), batch_size):
+        batches.append(leftover[k:k + batch_size])
+        uniform.append(0)
+    perm = np.array([i for bt in batches for i in bt], dtype=np.int32)
+    offsets = np.zeros(len(batches) + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum([len(bt) for bt in batches])
+    return perm, offsets, np.array(uniform, dtype=np.uint8), num_uniform
+
+
+def pool_gather(arena, slot_cols, slot_len, rows, scratch, pad_id: int = 0, pool_ids=None):
+    """Gather mixed-length pool rows into a left-padded batch (the "repad" of [BSDDR 2.2]
+    applied to EXSPEC's leftovers [BSDDR 2.3]).
+
+    arena:     [L, 2, H, C, hd]  the pool's K/V, unpadded at rest: slot s owns columns
+               [slot_cols[s], slot_cols[s] + capacity) and holds K/V of its first N_s - 1 tokens.
+    slot_len:  [S] committed length N_s per slot.
+    rows:      the batch's slots, in batch order.
+    scratch:   [L, 2, R, H, Sc, hd] padded batch buffer (R >= len(rows)).
+    Row i of the batch gets width W = max N_s over the batch; its K/V columns [0, N_s - 1) move to
+    scratch columns [W - N_s, W - 1).  Returns (scratch_out, W, ids, mask, pos) where ids is only
+    filled when ``pool_ids`` ([S, cap]) is given.
+    """
+    n = np.array([int(slot_len[s]) for s in rows], dtype=np.int64)
+    if (n < 1).any():
+        raise OracleError("empty sequence")
+    width = int(n.max())
+    out = np.array(scratch, copy=True)
+    Sc = scratch.shape[4]
+    ids = np.full((len(rows), Sc), pad_id, dtype=np.int32)
+    mask = np.zeros((len(rows), Sc), dtype=np.uint8)
+    pos = np.zeros((len(rows), Sc), dtype=np.int32)
+    for i, s in enumerate(rows):
+        c0 = int(slot_cols[s])
+        k = int(n[i]) - 1
+        d = width - int(n[i])
+        out[:, :, i, :, d:d + k, :] = arena[:, :, :, c0:c0 + k, :]
+        mask[i, d:width] = 1
+        pos[i, d:width] = np.arange(n[i])
+        if pool_ids is not None:
+            ids[i, d:width] = np.asarray(pool_ids[s, :n[i]])
+    return out, width, ids, mask, pos
+
+
+def pool_append(arena, slot_cols, slot_len, rows, scratch, width: int, accept_len, out_token,
+                draft, pool_ids=None):
+    """Append a verified batch back to its slots (the "append" of [BSDDR 2.2] for the pool).
+
+    Batch row i (slot s) keeps scratch columns [W - 1, W + a_i) (its pending token and accepted
+    drafts) which move to slot columns [N_s - 1, N_s + a_i); N_s grows by a_i + 1, and when
+    ``pool_ids`` is given the accepted drafts and the replacement/bonus token are appended to the
+    slot's ids.  Returns (arena_out, slot_len_out, pool_ids_out).
+    """
+    out = np.array(arena, copy=True)
+    new_len = np.array(slot_len, copy=True)
+    ids_out = None if pool_ids is None else np.array(pool_ids, copy=True)
+    for i, s in enumerate(rows):
+        a = int(accept_len[i])
+        nb = int(slot_len[s])
+        c0 = int(slot_cols[s])
+        out[:, :, :, c0 + nb - 1:c0 + nb + a, :] = scratch[:, :, i, :, width - 1:width + a, :]
+        new_len[s] = nb + a + 1
+        if ids_out is not None:
+            ids_out[s, nb:nb + a] = np.asarray(draft[i, :a])
+            ids_out[s, nb + a] = int(out_token[i])
+    return out, new_len, ids_out
