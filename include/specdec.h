@@ -1,0 +1,263 @@
+/*
+ * specdec.h -- C ABI of the GB300 (sm_103a) hot path of batch speculative decoding.
+ *
+ * One verification round of batched speculative decoding is:
+ *   1. verification of D draft tokens per sequence against the target's scores
+ *      (specdec_verify_greedy or specdec_verify_sample), giving an accept length a_b in [0, D]
+ *      and one replacement-or-bonus token y_b per row, and
+ *   2. realignment of the left-padded batch (specdec_realign): unpad every row, append the
+ *      a_b accepted drafts and y_b, re-left-pad to the longest row, rebuild the attention mask and
+ *      position IDs, and move every layer's surviving K/V columns, so that rectangular alignment
+ *      and position-ID contiguity hold again.
+ * For a pool of sequences, specdec_group_by_length forms batches of equal-length rows (which
+ * need no realignment) and batches of mixed leftovers, and specdec_pool_gather /
+ * specdec_pool_append move a mixed batch between the pool and a padded batch buffer.
+ *
+ * Sources (page title, section):
+ *   [IE5]   "Inference Engineering: Part 5/8: When Speculative Decoding Backfires"
+ *   [BSDDR] "Batch Speculative Decoding Done Right" (technical summary of arXiv 2510.22876)
+ *   [CF]    "Correctness Forensics for Batch Speculative Decoding: Diagnosing the Ragged Tensor
+ *           Problem", Abstract
+ *
+ * Conventions for every entry point:
+ *   - All array arguments are DEVICE pointers owned by the caller.  The library allocates no
+ *     memory and keeps no state between calls; calls on different streams are independent.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the legacy
+ *     default stream).  The return value reports host-detected problems only: an invalid
+ *     argument, an unsupported configuration, or a failed launch.  It does not wait for the GPU.
+ *   - Problems that only the GPU can see (a length, token or accept value out of range, a cache
+ *     too small for the new width) are reported through `dev_status`, a device int32 that the
+ *     caller zeroes beforehand: the kernel writes the first nonzero specdec_status it meets and
+ *     then writes no further outputs that depend on the bad value.  Kernels never trap, assert or
+ *     spin without bound; every wait has an iteration limit (SPECDEC_ERR_TIMEOUT).
+ *   - Integer outputs are bit-exact and deterministic.  Floating-point work is done in fp32 with
+ *     fp64 for the few cross-block combinations stated below.
+ */
+#ifndef SPECDEC_H
+#define SPECDEC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPECDEC_VERSION 100  /* 1.0.0 */
+#define SPECDEC_MAX_DRAFT 31 /* D <= 31: D+1 rows fit one warp ballot */
+
+typedef enum {
+  SPECDEC_OK = 0,
+  SPECDEC_ERR_INVALID_ARG = 1, /* host: NULL pointer, negative or inconsistent size, aliasing */
+  SPECDEC_ERR_UNSUPPORTED = 2, /* host: valid but outside this build's limits (sizes, alignment) */
+  SPECDEC_ERR_CUDA = 3,        /* host: a CUDA launch or attribute call failed */
+  SPECDEC_ERR_CAPACITY = 4,    /* device: the new width (+ D columns for the next pass) does not
+                                  fit the destination; nothing was moved */
+  SPECDEC_ERR_INPUT_RANGE = 5, /* device: a length, accept value, token id or uniform out of
+                                  range, or a score row with no comparable value (all NaN) */
+  SPECDEC_ERR_TIMEOUT = 6      /* device: a bounded wait on an asynchronous copy ran out */
+} specdec_status;
+
+typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype;
+
+/* Library version (SPECDEC_VERSION of the build). */
+int specdec_version(void);
+
+/* Static, human-readable name of a specdec_status value ("unknown status" otherwise). */
+const char* specdec_status_string(int status);
+
+/*
+ * Greedy verification.  [IE5, "Exactness Means Different Things For Greedy And Sampled Output"
+ * (greedy: accept while the draft equals the main model's highest-score token, replace the first
+ * mismatch with the main model's choice); "Draft Possible Tokens, Then Verify Them Together"
+ * (read left to right, discard everything after the first rejection, bonus token after a fully
+ * accepted draft); "One Verification Pass Can Commit Several Tokens" (worked example).]
+ *
+ *   logits     [B][D+1][row_stride] scores of the target (dtype F32 or BF16); row (b, j) holds
+ *              the scores of the token after draft j of row b (j = 0: after the last committed
+ *              token).  Only the first V elements of each row are read.  Element-aligned.
+ *   draft      [B][D] int32 draft tokens d_1..d_D.
+ *   accept_len [B] int32 out: a_b = number of leading drafts equal to the target's choice.
+ *   out_token  [B] int32 out: y_b = the target's choice at row a_b (the replacement when a_b < D,
+ *              the bonus token when a_b == D).  The cycle commits a_b + 1 tokens.
+ * The target's choice of a row is its maximum score, lowest token index on ties; NaN scores are
+ * never chosen (a row of only NaN sets SPECDEC_ERR_INPUT_RANGE).  A draft id outside [0, V) sets
+ * SPECDEC_ERR_INPUT_RANGE and counts as a mismatch.
+ * Limits: B >= 0, 1 <= D <= 31, 1 <= V, row_stride >= V.
+ */
+int specdec_verify_greedy(const void* logits, int dtype, int B, int D, int V,
+                          long long row_stride, const int32_t* draft, int32_t* accept_len,
+                          int32_t* out_token, int32_t* dev_status, void* stream);
+
+/*
+ * Sampled verification (speculative rejection sampling).  [IE5, "Exactness Means Different
+ * Things For Greedy And Sampled Output": accept a draft x with probability min(1, p(x)/q(x)); at
+ * a rejection draw the replacement from normalize(max(0, p - q)); both models use the same
+ * sampling settings.  "Draft Possible Tokens, Then Verify Them Together": left to right, the
+ * first rejection ends the cycle, the bonus comes from the distribution after the full draft.]
+ *
+ *   target_logits [B][D+1][row_stride] target scores; p_j = softmax(target row j / T).
+ *   draft_logits  [B][D][row_stride] draft-model scores; q_j = softmax(draft row j / T).
+ *   draft         [B][D] draft tokens (drawn from q by the draft model).
+ *   uniforms      [B][D+1] float32 in [0, 1): u[b][j] (j < D) decides draft j+1: accepted iff
+ *                 u < p_j(d)/q_j(d); u[b][D] drives the replacement / bonus draw.
+ *   accept_len, out_token  as for greedy verification.
+ *   residual_out  [B][V] float32 out, may be NULL: the normalised distribution y_b was drawn from
+ *                 (normalize(max(0, p_a - q_a)) after a rejection at a = a_b < D, p_D when all
+ *                 drafts were accepted).
+ * The draw is an inverse CDF over ascending token ids: the first k whose running sum exceeds
+ * u[b][D] * (total).  If max(0, p - q) is zero everywhere the draw uses p instead.
+ * Precision: exponentials and per-element probabilities in fp32; the acceptance ratio p(d)/q(d)
+ * and the cross-block normalisers in fp64.  Limits: B >= 0, 1 <= D <= 31, 1 <= V,
+ * row_stride >= V, temperature > 0 and finite.  Uniforms outside [0, 1) set
+ * SPECDEC_ERR_INPUT_RANGE.
+ */
+int specdec_verify_sample(const void* target_logits, const void* draft_logits, int dtype, int B,
+                          int D, int V, long long row_stride, float temperature,
+                          const int32_t* draft, const float* uniforms, int32_t* accept_len,
+                          int32_t* out_token, float* residual_out, int32_t* dev_status,
+                          void* stream);
+
+/*
+ * A view of a K/V cache in device memory.  Element (layer l, k-or-v kv, row r, head h,
+ * column c, e) lives at  base + l*stride_layer + kv*stride_kv + r*stride_row + h*stride_head
+ *                        + c*head_dim + e          (strides in elements).
+ * One column of one head (head_dim elements) is contiguous, and the columns of one
+ * (l, kv, r, h) are contiguous.  The natural layout [L][2][rows][H][cap_cols][head_dim] has
+ * stride_head = cap_cols*head_dim, stride_row = H*stride_head, stride_kv = rows*stride_row,
+ * stride_layer = 2*stride_kv.  `base` and head_dim*element size must be multiples of 16 bytes,
+ * and so must every stride times the element size.
+ */
+typedef struct {
+  void* base;
+  long long stride_layer, stride_kv, stride_row, stride_head;
+  int dtype; /* specdec_dtype of the elements (only the size matters: values are moved) */
+  int layers, rows, heads, head_dim, cap_cols;
+} specdec_kv_view;
+
+/*
+ * EQSPEC realignment (unpad, append, repad), out of place.  [BSDDR section 2.2 (unpad each row,
+ * append accepted and bonus tokens, left-pad to the longest row, recompute position IDs, shift
+ * the KV cache); section 2.1 (rectangular alignment: pad + content equal across the batch;
+ * position-ID contiguity: IDs from 0, contiguous over the mask's content); CF Abstract (the
+ * ragged tensor problem under contiguous layouts); IE5 "Acceptance changes across the workload"
+ * (keep committed K/V, discard speculative entries after the first rejection).]
+ *
+ * State before (width W = *width, N_b = n_committed[b] in [1, W]):
+ *   ids_src row b holds the N_b committed tokens at columns [W - N_b, W); src holds K/V for
+ *   columns [W - N_b, W - 1) (all committed tokens but the last, "pending" one) and for the D+1
+ *   columns [W - 1, W + D) the verification pass wrote for [pending, d_1 .. d_D].
+ * State after (N'_b = N_b + a_b + 1, W' = max_b N'_b):
+ *   dst columns [W' - N'_b, W' - 1) of every (layer, kv, head) of row b = src columns
+ *   [W - N_b, W + a_b) (the rejected drafts' columns [W + a_b, W + D) are not copied);
+ *   ids_dst row b = pad_id at [0, W' - N'_b), then the old committed tokens, d_1..d_{a_b} and
+ *   y_b ending at column W' - 1, pad_id again from W' on; mask_dst = 1 exactly on
+ *   [W' - N'_b, W'); pos_dst = 0, 1, .., N'_b - 1 there and 0 elsewhere; n_committed_dst = N';
+ *   *width_dst = W'.  dst pad columns are left as they were (unspecified).
+ * All per-row values are read on the device: no host synchronisation is needed between
+ * verification and realignment, and the call can be captured in a CUDA graph.
+ * Device-detected errors (no output is written): N_b outside [1, W] or a_b outside [0, D]
+ * (SPECDEC_ERR_INPUT_RANGE); W + D > src.cap_cols (SPECDEC_ERR_INPUT_RANGE); W' + D > dst.cap_cols
+ * (SPECDEC_ERR_CAPACITY: the next verification pass could not be written).
+ * src and dst must be distinct, non-overlapping buffers of equal geometry except cap_cols; the
+ * metadata outputs must not alias their inputs.  Limits: 0 <= B <= 1024 (B == src.rows ==
+ * dst.rows), 1 <= D <= 31.
+ */
+typedef struct {
+  specdec_kv_view src, dst;
+  int B, D;
+  int32_t pad_id;
+  int copy_engine;                /* 0: TMA bulk copies (default); 1: 16-byte vector loads */
+  const int32_t* n_committed;     /* [B]  N_b */
+  const int32_t* width;           /* [1]  W */
+  const int32_t* accept_len;      /* [B]  a_b */
+  const int32_t* out_token;       /* [B]  y_b */
+  const int32_t* draft;           /* [B][D] */
+  const int32_t* ids_src;         /* [B][src.cap_cols] */
+  int32_t* ids_dst;               /* [B][dst.cap_cols] */
+  uint8_t* mask_dst;              /* [B][dst.cap_cols] */
+  int32_t* pos_dst;               /* [B][dst.cap_cols] */
+  int32_t* n_committed_dst;       /* [B]  N'_b */
+  int32_t* width_dst;             /* [1]  W' */
+  int32_t* dev_status;            /* [1] */
+} specdec_realign_args;
+
+int specdec_realign(const specdec_realign_args* args, void* stream);
+
+/*
+ * EXSPEC grouping of a SequencePool by length.  [BSDDR section 2.3: keep a pool of active
+ * sequences; group same-length sequences so they need no realignment; only mixed-length ones are
+ * realigned.]
+ *
+ *   lengths       [N] int32 in [0, max_len]: committed length of each pool row.
+ *   perm          [N] int32 out: pool rows in batch order.
+ *   batch_offsets [N+1] int32 out: batch k is perm[batch_offsets[k] .. batch_offsets[k+1]).
+ *   batch_uniform [N] uint8 out: 1 for a uniform batch (batch_size rows of one length).
+ *   num_batches, num_uniform  [1] int32 out.
+ * Rule: a stable counting sort by length; rows of one length, in index order, fill whole batches
+ * of batch_size first (uniform batches, ascending length); the remaining rows of every length,
+ * in (length, index) order, are cut into mixed batches of batch_size rows (the last may be
+ * shorter).  Uniform batches come first.  Entries past num_batches are not written.
+ * Limits: 0 <= N <= 4096, batch_size >= 1, 0 <= max_len <= 16383.  A length outside
+ * [0, max_len] sets SPECDEC_ERR_INPUT_RANGE (no output written).
+ */
+int specdec_group_by_length(const int32_t* lengths, int N, int batch_size, int max_len,
+                            int32_t* perm, int32_t* batch_offsets, uint8_t* batch_uniform,
+                            int32_t* num_batches, int32_t* num_uniform, int32_t* dev_status,
+                            void* stream);
+
+/*
+ * Pool <-> padded-batch moves for EXSPEC's mixed leftovers.  [BSDDR section 2.3 (only
+ * mixed-length sequences are realigned) with the unpad-append-repad of section 2.2.]
+ *
+ * The pool is unpadded at rest: slot s owns arena columns [slot_col[s], slot_col[s] +
+ * slot_cap[s]) of row 0 of `arena`, and holds K/V for its first N_s - 1 tokens (all but the
+ * pending one) at the start of that range; pool_ids[s][0 .. N_s) are its tokens.
+ *
+ * specdec_pool_gather (repad): for the k = n_rows slots rows[0..k) with W = max N_s:
+ *   scratch row i columns [W - N_s, W - 1) = the slot's K/V columns [0, N_s - 1);
+ *   scratch_ids / scratch_mask / scratch_pos row i = the left-padded batch of width W (as
+ *   specdec_realign writes them); batch_len[i] = N_s; *width = W.
+ *   in_place != 0 (a uniform batch, all N_s equal): no K/V or metadata is moved; only batch_len
+ *   and *width are written (the verification pass can work on the slots directly).
+ *   Errors: N_s < 1 or N_s > slot_cap[s] (INPUT_RANGE); W + D > scratch.cap_cols, or N_s + D >
+ *   slot_cap[s] (CAPACITY).
+ * specdec_pool_append (append): after the verification pass wrote columns [W - 1, W + D) of
+ *   every scratch row (or, in place, slot columns [N_s - 1, N_s + D)) and verification gave
+ *   accept_len[i], out_token[i] in batch-row order:
+ *   slot columns [N_s - 1, N_s + a_i) = scratch row i columns [W - 1, W + a_i) (not copied in
+ *   place); pool_ids[s][N_s .. N_s + a_i) = d_1..d_{a_i}, pool_ids[s][N_s + a_i] = y_i;
+ *   slot_len[s] = N_s + a_i + 1, with N_s = batch_len[i] as the gather recorded it.
+ *   Errors: a_i outside [0, D] (INPUT_RANGE; nothing written).
+ * Limits: 1 <= n_rows <= min(1024, scratch.rows), 1 <= D <= 31, arena.rows == 1, arena and
+ * scratch of equal layers, heads, head_dim and element size.  Rows must name distinct slots.
+ */
+typedef struct {
+  specdec_kv_view arena;        /* the pool's K/V (rows == 1) */
+  specdec_kv_view scratch;      /* padded batch buffer [L][2][R][H][Sc][hd] */
+  int n_rows, D;
+  int32_t pad_id;
+  int in_place;                 /* uniform batch: verification works on the slots directly */
+  const int32_t* rows;          /* [n_rows] slot of each batch row */
+  const int32_t* slot_col;      /* [S] first arena column of each slot */
+  const int32_t* slot_cap;      /* [S] arena columns owned by each slot */
+  int32_t* slot_len;            /* [S] N_s (read by gather; advanced by append) */
+  int32_t* pool_ids;            /* [S][ids_cap] tokens of each slot */
+  int ids_cap;
+  int32_t* batch_len;           /* [n_rows] N_s recorded by gather, read by append */
+  int32_t* width;               /* [1] W written by gather, read by append */
+  int32_t* scratch_ids;         /* [R][Sc] written by gather (may be NULL when in_place) */
+  uint8_t* scratch_mask;        /* [R][Sc] */
+  int32_t* scratch_pos;         /* [R][Sc] */
+  const int32_t* accept_len;    /* [n_rows] append only */
+  const int32_t* out_token;     /* [n_rows] append only */
+  const int32_t* draft;         /* [n_rows][D] append only */
+  int32_t* dev_status;          /* [1] */
+} specdec_pool_args;
+
+int specdec_pool_gather(const specdec_pool_args* args, void* stream);
+int specdec_pool_append(const specdec_pool_args* args, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECDEC_H */

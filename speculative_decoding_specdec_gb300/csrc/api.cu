@@ -1,0 +1,44 @@
+// Library-wide entry points (version, status names) and host helpers shared by the kernels.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace specdec {
+
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+int map_cuda_error(cudaError_t e) {
+  if (e == cudaSuccess) return SPECDEC_OK;
+  (void)cudaGetLastError();  // clear a non-sticky launch error so later calls start clean
+  return SPECDEC_ERR_CUDA;
+}
+
+}  // namespace specdec
+
+extern "C" int specdec_version(void) { return SPECDEC_VERSION; }
+
+extern "C" const char* specdec_status_string(int status) {
+  switch (status) {
+    case SPECDEC_OK: return "ok";
+    case SPECDEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPECDEC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SPECDEC_ERR_CUDA: return "CUDA launch or attribute call failed";
+    case SPECDEC_ERR_CAPACITY: return "destination capacity exceeded";
+    case SPECDEC_ERR_INPUT_RANGE: return "input value out of range";
+    case SPECDEC_ERR_TIMEOUT: return "bounded wait on an asynchronous copy ran out";
+    default: return "unknown status";
+  }
+}
