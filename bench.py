@@ -1,0 +1,423 @@
+"""Benchmark of the verify + realign hot path (one step = one speculative round).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload vicuna7b|qwen3_8b|glm4_9b]
+                    [--impl specdec|reference] [--copy-engine 0|1]
+
+A step is one round: verification of the round's D drafts per row against the target's scores,
+then realignment of the left-padded batch (every layer's surviving K/V columns move to the other
+cache buffer, ids/mask/position IDs are rebuilt).  Inputs are synthetic, seeded and resident on
+the device before the timed region; every round streams gigabytes of K/V, far more than L2.
+With --gpus N (under torchrun) every rank runs an independent replica of the workload (the path
+has no exchange step); ``value`` is the rounds of all ranks over the slowest rank's time.
+
+--impl reference times the CPU oracle (plain numpy, float64) on this host on a bounded sample of
+the same workload; it is the deliberately slow baseline, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify+realign rounds/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=40)
+    p.add_argument("--warmup", type=int, default=4)
+    p.add_argument("--workload", default="vicuna7b")
+    p.add_argument("--impl", default="specdec", choices=["specdec", "reference"])
+    p.add_argument("--copy-engine", type=int, default=0)
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------------------ distributed
+
+def dist_setup(gpus):
+    import torch
+    import torch.distributed as dist
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    """Largest value of ``x`` over all ranks (the slowest rank's time)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        else:
+            self.lines = []
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+def run_specdec(args, rank, ws, local):
+    import numpy as np
+    import torch
+    from speculative_decoding_specdec_gb300 import synth
+    from speculative_decoding_specdec_gb300.engine import EqspecBatch
+
+    w = synth.WORKLOADS[args.workload]
+    if w.mode == "pool":
+        raise SystemExit("the pool workload is benchmarked by its own script section (not yet)")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    K, Wm = args.steps, args.warmup
+    R = K + Wm
+    gen_cpu = synth.make_gen(w.seed * 1000 + rank)
+    n0 = w.prompt_lengths(gen_cpu)
+    prompts = [torch.randint(0, w.V, (int(n),), generator=gen_cpu).tolist() for n in n0]
+    cap = w.capacity(int(n0.max()), rounds=R)
+    eng = EqspecBatch(w.layers, w.heads, w.head_dim, w.kv_dtype, w.B, w.D, cap, R, device=dev)
+    g = torch.Generator(device=dev).manual_seed(w.seed * 7919 + rank)
+    for k in eng.kv:
+        k.normal_(generator=g)
+    # all rounds' inputs, generated before any timed region
+    logits, drafts, draft_logits, uniforms = [], [], [], []
+    for _ in range(R):
+        if w.mode == "greedy":
+            lg, d = synth.greedy_round(g, w.B, w.D, w.V, w.alpha, dtype=w.logit_dtype, device=dev)
+        else:
+            lg, dl, d, u = synth.sampled_round(g, w.B, w.D, w.V, w.temperature,
+                                               dtype=w.logit_dtype, device=dev)
+            draft_logits.append(dl)
+            uniforms.append(u)
+        logits.append(lg)
+        drafts.append(d)
+    stream = torch.cuda.current_stream()
+
+    def verify(r, lg=None, d=None):
+        lg = logits[r] if lg is None else lg
+        d = drafts[r] if d is None else d
+        if w.mode == "greedy":
+            eng.verify_greedy(lg, d)
+        else:
+            eng.verify_sample(lg, draft_logits[r], d, uniforms[r], w.temperature)
+
+    # ---------------- device-resident timing
+    eng.start(prompts)
+    for r in range(Wm):
+        verify(r)
+        eng.realign(drafts[r], copy_engine=args.copy_engine)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t0.record(stream)
+        for i in range(K):
+            r = Wm + i
+            ev[i][0].record(stream)
+            verify(r)
+            ev[i][1].record(stream)
+            eng.realign(drafts[r], copy_engine=args.copy_engine)
+            ev[i][2].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    ms = t0.elapsed_time(t1)
+    status = int(eng.status.item())
+    if status:
+        raise RuntimeError(f"device status {status} during the timed rounds")
+    t_verify = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    t_realign = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    n_hist = eng.n_hist.cpu().numpy().astype(np.int64)
+    acc = [(n_hist[r + 1] - n_hist[r] - 1) for r in range(Wm, R)]
+    moved_cols = sum(int((n_hist[r + 1] - 1).sum()) for r in range(Wm, R))  # N'_b - 1 per row
+    realign_bytes = 2.0 * moved_cols * w.token_bytes / K
+    es = torch.tensor([], dtype=w.logit_dtype).element_size()
+    verify_bytes = (w.B * (w.D + 1) * w.V * es + (w.B * w.D * w.V * es if w.mode == "sampled" else 0)
+                    + w.B * w.D * 4 + w.B * 8)
+    committed = float(sum(int(a.sum()) + len(a) for a in acc)) / K
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin_lg = [x.cpu().pin_memory() for x in logits]
+        pin_d = [x.cpu().pin_memory() for x in drafts]
+        pin_dl = [x.cpu().pin_memory() for x in draft_logits]
+        pin_u = [x.cpu().pin_memory() for x in uniforms]
+        dev_lg = torch.empty_like(logits[0])
+        dev_d = torch.empty_like(drafts[0])
+        dev_dl = torch.empty_like(draft_logits[0]) if draft_logits else None
+        dev_u = torch.empty_like(uniforms[0]) if uniforms else None
+        out = torch.empty((K, 2 * w.B + w.B + 1), dtype=torch.int32).pin_memory()
+        eng.start(prompts)
+
+        def e2e_round(r, i):
+            dev_lg.copy_(pin_lg[r], non_blocking=True)
+            dev_d.copy_(pin_d[r], non_blocking=True)
+            if w.mode == "greedy":
+                eng.verify_greedy(dev_lg, dev_d)
+            else:
+                dev_dl.copy_(pin_dl[r], non_blocking=True)
+                dev_u.copy_(pin_u[r], non_blocking=True)
+                eng.verify_sample(dev_lg, dev_dl, dev_d, dev_u, w.temperature)
+            eng.realign(dev_d, copy_engine=args.copy_engine)
+            if i is not None:
+                out[i, :w.B].copy_(eng.accept_len, non_blocking=True)
+                out[i, w.B:2 * w.B].copy_(eng.out_token, non_blocking=True)
+                out[i, 2 * w.B:3 * w.B].copy_(eng.n_committed, non_blocking=True)
+                out[i, 3 * w.B:].copy_(eng.width, non_blocking=True)
+
+        for r in range(Wm):
+            e2e_round(r, None)
+        torch.cuda.synchronize()
+        barrier(ws)
+        torch.cuda.synchronize()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for i in range(K):
+            e2e_round(Wm + i, i)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e2e_ms = max_over_ranks(s0.elapsed_time(s1), ws)
+        h2d = sum(x.numel() * x.element_size() for x in
+                  [pin_lg[0], pin_d[0]] + ([pin_dl[0], pin_u[0]] if pin_dl else []))
+        e2e = {"value": K * ws / (e2e_ms / 1e3), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": out[0].numel() * 4}
+
+    ms_max = max_over_ranks(ms, ws)
+    rounds_all = sum_over_ranks(float(K), ws)
+    peak, peak_kind = measured_peaks()
+    achieved = realign_bytes / (t_realign / 1e3) / 1e9
+    verify_gbs = verify_bytes / (t_verify / 1e3) / 1e9
+    return {
+        "value": rounds_all / (ms_max / 1e3),
+        "ms_per_step": ms_max / K,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+        "roofline": {"bound": "hbm", "kernel": "realign", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "bytes_per_launch": realign_bytes, "ms_per_launch": t_realign},
+        "verify": {"ms_per_launch": t_verify, "bytes_per_launch": verify_bytes,
+                   "achieved_gbs": round(verify_gbs, 1), "frac": round(verify_gbs / peak, 4)},
+        "committed_slots_per_s": committed / (ms_max / K / 1e3),
+        "committed_per_round": committed,
+        "cap_cols": cap,
+    }
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+
+def oracle_round_sampler(wname, seed=0, layers_sample=2):
+    """A bounded sample of the workload for the oracle: full verification of every row, and
+    realignment of ``layers_sample`` of the layers (scaled to all layers)."""
+    import numpy as np
+    import torch
+    from oracle import specdec_oracle as O
+    from speculative_decoding_specdec_gb300 import synth
+
+    w = synth.WORKLOADS[wname]
+    gen = synth.make_gen(w.seed * 1000 + seed)
+    n = w.prompt_lengths(gen).numpy().astype(np.int64)
+    W = int(n.max())
+    cap = w.capacity(W, rounds=64)
+    Ls = min(layers_sample, w.layers)
+    rng = np.random.default_rng(seed)
+    kv = [rng.integers(-30000, 30000, size=(Ls, 2, w.B, w.heads, cap, w.head_dim),
+                       dtype=np.int16) for _ in range(2)]
+    ids = np.zeros((w.B, cap), np.int32)
+    state = {"n": n, "W": W, "ids": ids, "cur": 0}
+
+    def one_round():
+        """Returns (verify seconds, realign seconds); input generation is not timed."""
+        if w.mode == "greedy":
+            lg, d = synth.greedy_round(gen, w.B, w.D, w.V, w.alpha, dtype=w.logit_dtype)
+            lg64 = lg.double().numpy()
+            t0 = time.perf_counter()
+            a, y = O.verify_greedy(lg64, d.numpy())
+        else:
+            lg, dl, d, u = synth.sampled_round(gen, w.B, w.D, w.V, w.temperature,
+                                               dtype=w.logit_dtype)
+            lg64, dl64, u64 = lg.double().numpy(), dl.double().numpy(), u.double().numpy()
+            t0 = time.perf_counter()
+            a, y, _, _ = O.verify_sample(lg64, dl64, d.numpy(), u64, w.temperature)
+        t1 = time.perf_counter()
+        c = state["cur"]
+        out, ids2, _, _, n2, W2 = O.realign(kv[c], kv[1 - c], state["n"], state["W"], a, y,
+                                            d.numpy(), state["ids"], 0)
+        t2 = time.perf_counter()
+        kv[1 - c] = out
+        state.update(n=n2.astype(np.int64), W=W2, ids=ids2, cur=1 - c)
+        return t1 - t0, t2 - t1
+
+    return w, Ls, one_round
+
+
+def time_oracle(wname, budget_s=15.0, max_rounds=None):
+    """Rounds/s of the oracle on a bounded sample (verify timed whole, realign on a layer sample
+    scaled to all layers)."""
+    w, Ls, one_round = oracle_round_sampler(wname)
+    total, rounds = 0.0, 0
+    start = time.perf_counter()
+    while True:
+        t_verify, t_realign = one_round()
+        total += t_verify + t_realign * (w.layers / Ls)
+        rounds += 1
+        if time.perf_counter() - start > budget_s or (max_rounds and rounds >= max_rounds):
+            break
+    return rounds / total, rounds, Ls, w
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return None
+    rps, rounds, Ls, w = time_oracle(args.workload, budget_s=max(10.0, 2.0 * args.steps),
+                                     max_rounds=args.warmup + args.steps)
+    sample = (f"{rounds} rounds of {w.name}: verification of all {w.B} rows, realignment of "
+              f"{Ls} of {w.layers} layers scaled x{w.layers / Ls:g}")
+    return {"value": rps, "cpu_baseline": {"value": rps, "unit": "rounds/s", "cores": 1,
+                                           "kind": "oracle", "sample": sample}}
+
+
+# ------------------------------------------------------------------------------ main
+
+def main():
+    args = parse()
+    rank, ws, local = dist_setup(args.gpus)
+    from speculative_decoding_specdec_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    config = {"workload": f"{w.name}: L={w.layers} KV heads={w.heads} head_dim={w.head_dim} "
+                          f"B={w.B} D={w.D} V={w.V} {w.mode} verify",
+              "B": w.B, "D": w.D, "V": w.V, "layers": w.layers, "kv_heads": w.heads,
+              "head_dim": w.head_dim, "verify": w.mode,
+              "l2": "inputs larger than L2: every round streams >= 1 GB of K/V; all rounds' "
+                    "score rows are distinct and generated before the timed region",
+              "parallelism": f"replicas x{ws}"}
+    line = {"metric": METRIC, "unit": "rounds/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config}
+    if args.impl == "reference":
+        res = run_reference(args, rank, ws)
+        if rank == 0:
+            line.update(impl="reference", value=res["value"], ms_per_step=1e3 / res["value"],
+                        cpu_baseline=res["cpu_baseline"], dtype="f64",
+                        e2e={"value": res["value"], "unit": "rounds/s",
+                             "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0})
+            print(json.dumps(line))
+        return
+    res = run_specdec(args, rank, ws, local)
+    if rank == 0:
+        cpu = None
+        if ws == 1:
+            rps, rounds, Ls, _ = time_oracle(args.workload, budget_s=12.0)
+            cpu = {"value": rps, "unit": "rounds/s", "cores": 1, "kind": "oracle",
+                   "sample": f"{rounds} rounds: verification of all rows, realignment of {Ls} of "
+                             f"{w.layers} layers scaled x{w.layers / Ls:g}"}
+        line.update(value=res["value"], ms_per_step=res["ms_per_step"], clocks=res["clocks"],
+                    e2e=res["e2e"], roofline=res["roofline"], verify=res["verify"],
+                    committed_token_slots_per_s=res["committed_slots_per_s"],
+                    committed_per_round=res["committed_per_round"], gpu_launches=2 * args.steps,
+                    cpu_baseline=cpu)
+        line["config"]["cap_cols"] = res["cap_cols"]
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

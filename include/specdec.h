@@ -219,15 +219,16 @@ int specdec_group_by_length(const int32_t* lengths, int N, int batch_size, int m
  *   specdec_realign writes them); batch_len[i] = N_s; *width = W.
  *   in_place != 0 (a uniform batch, all N_s equal): no K/V or metadata is moved; only batch_len
  *   and *width are written (the verification pass can work on the slots directly).
- *   Errors: N_s < 1 or N_s > slot_cap[s] (INPUT_RANGE); W + D > scratch.cap_cols, or N_s + D >
- *   slot_cap[s] (CAPACITY).
+ *   Errors: N_s < 1, N_s > slot_cap[s], or a slot range outside the arena (INPUT_RANGE);
+ *   W + D > scratch.cap_cols, or N_s + D > slot_cap[s] (CAPACITY).
  * specdec_pool_append (append): after the verification pass wrote columns [W - 1, W + D) of
  *   every scratch row (or, in place, slot columns [N_s - 1, N_s + D)) and verification gave
  *   accept_len[i], out_token[i] in batch-row order:
  *   slot columns [N_s - 1, N_s + a_i) = scratch row i columns [W - 1, W + a_i) (not copied in
  *   place); pool_ids[s][N_s .. N_s + a_i) = d_1..d_{a_i}, pool_ids[s][N_s + a_i] = y_i;
  *   slot_len[s] = N_s + a_i + 1, with N_s = batch_len[i] as the gather recorded it.
- *   Errors: a_i outside [0, D] (INPUT_RANGE; nothing written).
+ *   Errors: a_i outside [0, D], a recorded width/length out of range (INPUT_RANGE; nothing
+ *   written).
  * Limits: 1 <= n_rows <= min(1024, scratch.rows), 1 <= D <= 31, arena.rows == 1, arena and
  * scratch of equal layers, heads, head_dim and element size.  Rows must name distinct slots.
  */

@@ -80,7 +80,7 @@ struct Params {
   int32_t* s_ids;
   uint8_t* s_mask;
   int32_t* s_pos;
-  int scratch_cap;
+  int scratch_cap, arena_cap;
   int32_t* status;
 };
 
@@ -157,8 +157,8 @@ __device__ bool build_plan(const Params& p, Plan& s, int* red) {
   } else if (p.mode == kPoolGather) {
     for (int r = threadIdx.x; r < R; r += kThreads) {
       const int sl = p.rows[r];
-      const int N = p.slot_len[sl], cap = p.slot_cap[sl];
-      if (N < 1 || N > cap || N > p.ids_cap) bad |= 1;
+      const int N = p.slot_len[sl], cap = p.slot_cap[sl], c0 = p.slot_col[sl];
+      if (N < 1 || N > cap || N > p.ids_cap || c0 < 0 || cap > p.arena_cap - c0) bad |= 1;
       else if (N + D > cap) bad |= 2;
       s.aux[r] = N;
       mx = max(mx, N);
@@ -176,11 +176,13 @@ __device__ bool build_plan(const Params& p, Plan& s, int* red) {
     const int W = *p.bwidth;
     for (int r = threadIdx.x; r < R; r += kThreads) {
       const int N = p.batch_len[r], a = p.accept_len[r];
-      if (a < 0 || a > D || N < 1 || N > W) bad |= 1;
-      else if (N + a + 1 > p.ids_cap || N + a > p.slot_cap[p.rows[r]]) bad |= 2;
+      const int sl = p.rows[r], c0 = p.slot_col[sl], cap = p.slot_cap[sl];
+      if (a < 0 || a > D || N < 1 || N > W || c0 < 0 || cap > p.arena_cap - c0) bad |= 1;
+      else if (N + a + 1 > p.ids_cap || N + a > cap) bad |= 2;
       s.aux[r] = N;
       s.acc[r] = a;
     }
+    if (!p.in_place && (W < 1 || W + D > p.scratch_cap)) bad |= 1;
     block_max_or(mx, bad, red);
     if (threadIdx.x == 0) { s.W = W; s.Wp = W; }
     for (int r = threadIdx.x; r < R; r += kThreads) {
@@ -539,6 +541,7 @@ int pool_common(const specdec_pool_args* a, Params& p, bool append) {
   p.s_mask = a->scratch_mask;
   p.s_pos = a->scratch_pos;
   p.scratch_cap = sc.cap_cols;
+  p.arena_cap = ar.cap_cols;
   p.status = a->dev_status;
   return SPECDEC_OK;
 }

@@ -1,0 +1,268 @@
+"""ctypes binding of libspecdec.so (see include/specdec.h for the full contract).
+
+Argument marshalling only: tensors become device pointers, strides and sizes; every step runs in
+the library's CUDA kernels.  Importing this module raises ImportError when the library has not
+been built -- there is no fallback.  Host-detected errors raise SpecdecError; device-detected
+errors land in the caller's ``status`` tensor (zero it before the call, read it when convenient).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecdec.so")
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                      "(or python -m speculative_decoding_specdec_gb300._build)")
+lib = ctypes.CDLL(LIB_PATH)
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_CAPACITY, ERR_INPUT_RANGE, ERR_TIMEOUT = range(7)
+F32, BF16 = 0, 1
+MAX_DRAFT = 31
+
+c_i32p = ctypes.POINTER(ctypes.c_int32)
+
+
+class KvView(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p),
+                ("stride_layer", ctypes.c_longlong), ("stride_kv", ctypes.c_longlong),
+                ("stride_row", ctypes.c_longlong), ("stride_head", ctypes.c_longlong),
+                ("dtype", ctypes.c_int), ("layers", ctypes.c_int), ("rows", ctypes.c_int),
+                ("heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("cap_cols", ctypes.c_int)]
+
+
+class RealignArgs(ctypes.Structure):
+    _fields_ = [("src", KvView), ("dst", KvView), ("B", ctypes.c_int), ("D", ctypes.c_int),
+                ("pad_id", ctypes.c_int32), ("copy_engine", ctypes.c_int),
+                ("n_committed", ctypes.c_void_p), ("width", ctypes.c_void_p),
+                ("accept_len", ctypes.c_void_p), ("out_token", ctypes.c_void_p),
+                ("draft", ctypes.c_void_p), ("ids_src", ctypes.c_void_p),
+                ("ids_dst", ctypes.c_void_p), ("mask_dst", ctypes.c_void_p),
+                ("pos_dst", ctypes.c_void_p), ("n_committed_dst", ctypes.c_void_p),
+                ("width_dst", ctypes.c_void_p), ("dev_status", ctypes.c_void_p)]
+
+
+class PoolArgs(ctypes.Structure):
+    _fields_ = [("arena", KvView), ("scratch", KvView), ("n_rows", ctypes.c_int),
+                ("D", ctypes.c_int), ("pad_id", ctypes.c_int32), ("in_place", ctypes.c_int),
+                ("rows", ctypes.c_void_p), ("slot_col", ctypes.c_void_p),
+                ("slot_cap", ctypes.c_void_p), ("slot_len", ctypes.c_void_p),
+                ("pool_ids", ctypes.c_void_p), ("ids_cap", ctypes.c_int),
+                ("batch_len", ctypes.c_void_p), ("width", ctypes.c_void_p),
+                ("scratch_ids", ctypes.c_void_p), ("scratch_mask", ctypes.c_void_p),
+                ("scratch_pos", ctypes.c_void_p), ("accept_len", ctypes.c_void_p),
+                ("out_token", ctypes.c_void_p), ("draft", ctypes.c_void_p),
+                ("dev_status", ctypes.c_void_p)]
+
+
+_vp, _ll, _i, _f = ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_float
+lib.specdec_version.restype = _i
+lib.specdec_version.argtypes = []
+lib.specdec_status_string.restype = ctypes.c_char_p
+lib.specdec_status_string.argtypes = [_i]
+lib.specdec_verify_greedy.restype = _i
+lib.specdec_verify_greedy.argtypes = [_vp, _i, _i, _i, _i, _ll, _vp, _vp, _vp, _vp, _vp]
+lib.specdec_realign.restype = _i
+lib.specdec_realign.argtypes = [ctypes.POINTER(RealignArgs), _vp]
+lib.specdec_group_by_length.restype = _i
+lib.specdec_group_by_length.argtypes = [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+lib.specdec_pool_gather.restype = _i
+lib.specdec_pool_gather.argtypes = [ctypes.POINTER(PoolArgs), _vp]
+lib.specdec_pool_append.restype = _i
+lib.specdec_pool_append.argtypes = [ctypes.POINTER(PoolArgs), _vp]
+if hasattr(lib, "specdec_verify_sample"):
+    lib.specdec_verify_sample.restype = _i
+    lib.specdec_verify_sample.argtypes = [_vp, _vp, _i, _i, _i, _i, _ll, _f, _vp, _vp, _vp, _vp,
+                                          _vp, _vp, _vp]
+
+
+class SpecdecError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {status_string(code)} (status {code})")
+        self.code = code
+
+
+def version() -> int:
+    return lib.specdec_version()
+
+
+def status_string(code: int) -> str:
+    return lib.specdec_status_string(int(code)).decode()
+
+
+def _check(rc, what):
+    if rc != OK:
+        raise SpecdecError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return F32
+    if dt == torch.bfloat16:
+        return BF16
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+
+
+def kv_view(t: torch.Tensor) -> KvView:
+    """View of a cache tensor shaped [L, 2, rows, H, cap, head_dim] whose last two dims are
+    contiguous (a column of a head is contiguous and columns follow each other)."""
+    if t.dim() != 6 or t.shape[1] != 2:
+        raise ValueError("cache must be [L, 2, rows, H, cap, head_dim]")
+    L, _, R, H, S, hd = t.shape
+    if t.stride(5) != 1 or t.stride(4) != hd:
+        raise ValueError("cache columns must be contiguous")
+    return KvView(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2), t.stride(3),
+                  dtype_code(t.dtype), L, R, H, hd, S)
+
+
+def _score_rows(x, B, rows, name):
+    """(row_stride) of a [B, rows, V] score tensor whose rows are evenly spaced."""
+    if x.dim() != 3 or x.shape[0] != B or x.shape[1] != rows:
+        raise ValueError(f"{name}: expected [B, {rows}, V], got {tuple(x.shape)}")
+    if x.stride(2) != 1 or (B > 1 and x.stride(0) != rows * x.stride(1)):
+        raise ValueError(f"{name}: rows must be evenly spaced with unit element stride")
+    return x.stride(1)
+
+
+def verify_greedy(logits, draft, accept_len, out_token, status, stream=None):
+    """Greedy verification: logits [B, D+1, V] (fp32/bf16), draft [B, D] int32 ->
+    accept_len[B], out_token[B] int32 (written asynchronously on ``stream``)."""
+    B, D = draft.shape
+    V = logits.shape[-1]
+    rs = _score_rows(logits, B, D + 1, "logits")
+    for t, n in ((draft, "draft"), (accept_len, "accept_len"), (out_token, "out_token"),
+                 (status, "status")):
+        _need(t, torch.int32, n)
+    _check(lib.specdec_verify_greedy(_ptr(logits), dtype_code(logits.dtype), B, D, V, rs,
+                                     _ptr(draft), _ptr(accept_len), _ptr(out_token), _ptr(status),
+                                     _stream(stream)), "specdec_verify_greedy")
+
+
+def verify_sample(target_logits, draft_logits, draft, uniforms, temperature, accept_len,
+                  out_token, status, residual=None, stream=None):
+    """Sampled verification (min(1, p/q) acceptance, normalised max(0, p - q) residual draw)."""
+    B, D = draft.shape
+    V = target_logits.shape[-1]
+    rs = _score_rows(target_logits, B, D + 1, "target_logits")
+    rs2 = _score_rows(draft_logits, B, D, "draft_logits")
+    if rs != rs2 or draft_logits.dtype != target_logits.dtype or draft_logits.shape[-1] != V:
+        raise ValueError("target and draft scores must share dtype, V and row stride")
+    _need(uniforms, torch.float32, "uniforms")
+    if tuple(uniforms.shape) != (B, D + 1) or not uniforms.is_contiguous():
+        raise ValueError("uniforms must be a contiguous [B, D+1] float32 tensor")
+    if residual is not None:
+        _need(residual, torch.float32, "residual")
+        if tuple(residual.shape) != (B, V) or not residual.is_contiguous():
+            raise ValueError("residual must be a contiguous [B, V] float32 tensor")
+    _check(lib.specdec_verify_sample(_ptr(target_logits), _ptr(draft_logits),
+                                     dtype_code(target_logits.dtype), B, D, V, rs,
+                                     float(temperature), _ptr(draft), _ptr(uniforms),
+                                     _ptr(accept_len), _ptr(out_token), _ptr(residual),
+                                     _ptr(status), _stream(stream)), "specdec_verify_sample")
+
+
+def realign(src, dst, n_committed, width, accept_len, out_token, draft, ids_src, ids_dst,
+            mask_dst, pos_dst, n_committed_dst, width_dst, status, pad_id=0, copy_engine=0,
+            stream=None):
+    """EQSPEC realignment from cache ``src`` into cache ``dst`` (both [L, 2, B, H, cap, hd])."""
+    B, D = draft.shape
+    a = RealignArgs()
+    a.src = kv_view(src)
+    a.dst = kv_view(dst)
+    a.B, a.D, a.pad_id, a.copy_engine = B, D, int(pad_id), int(copy_engine)
+    for name, t in (("n_committed", n_committed), ("width", width), ("accept_len", accept_len),
+                    ("out_token", out_token), ("draft", draft), ("ids_src", ids_src),
+                    ("ids_dst", ids_dst), ("pos_dst", pos_dst),
+                    ("n_committed_dst", n_committed_dst), ("width_dst", width_dst),
+                    ("dev_status", status)):
+        _need(t, torch.int32, name)
+        setattr(a, name, t.data_ptr())
+    _need(mask_dst, torch.uint8, "mask_dst")
+    a.mask_dst = mask_dst.data_ptr()
+    if ids_src.shape != (B, src.shape[4]) or not ids_src.is_contiguous():
+        raise ValueError("ids_src must be a contiguous [B, src cap] int32 tensor")
+    for t, n in ((ids_dst, "ids_dst"), (mask_dst, "mask_dst"), (pos_dst, "pos_dst")):
+        if t.shape != (B, dst.shape[4]) or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous [B, dst cap] tensor")
+    _check(lib.specdec_realign(ctypes.byref(a), _stream(stream)), "specdec_realign")
+
+
+def group_by_length(lengths, batch_size, max_len, perm, batch_offsets, batch_uniform,
+                    num_batches, num_uniform, status, stream=None):
+    """EXSPEC grouping of pool rows by length (stable counting sort, uniform batches first)."""
+    N = lengths.numel()
+    for t, n in ((lengths, "lengths"), (perm, "perm"), (batch_offsets, "batch_offsets"),
+                 (num_batches, "num_batches"), (num_uniform, "num_uniform"), (status, "status")):
+        _need(t, torch.int32, n)
+    _need(batch_uniform, torch.uint8, "batch_uniform")
+    if perm.numel() < N or batch_offsets.numel() < N + 1 or batch_uniform.numel() < N:
+        raise ValueError("output buffers too small")
+    _check(lib.specdec_group_by_length(_ptr(lengths), N, int(batch_size), int(max_len),
+                                       _ptr(perm), _ptr(batch_offsets), _ptr(batch_uniform),
+                                       _ptr(num_batches), _ptr(num_uniform), _ptr(status),
+                                       _stream(stream)), "specdec_group_by_length")
+
+
+def _pool_args(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len, width,
+               status, pad_id, in_place):
+    a = PoolArgs()
+    a.arena = kv_view(arena)
+    a.scratch = kv_view(scratch)
+    a.n_rows, a.D, a.pad_id, a.in_place = rows.numel(), int(D), int(pad_id), int(bool(in_place))
+    for name, t in (("rows", rows), ("slot_col", slot_col), ("slot_cap", slot_cap),
+                    ("slot_len", slot_len), ("pool_ids", pool_ids), ("batch_len", batch_len),
+                    ("width", width), ("dev_status", status)):
+        _need(t, torch.int32, name)
+        setattr(a, name, t.data_ptr())
+    if pool_ids.dim() != 2 or not pool_ids.is_contiguous():
+        raise ValueError("pool_ids must be a contiguous [slots, ids_cap] int32 tensor")
+    a.ids_cap = pool_ids.shape[1]
+    return a
+
+
+def pool_gather(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len, width,
+                status, scratch_ids=None, scratch_mask=None, scratch_pos=None, pad_id=0,
+                in_place=False, stream=None):
+    """Gather pool slots ``rows`` into the padded batch buffer ``scratch`` (see specdec.h)."""
+    a = _pool_args(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len,
+                   width, status, pad_id, in_place)
+    if not in_place:
+        for t, n, dt in ((scratch_ids, "scratch_ids", torch.int32),
+                         (scratch_mask, "scratch_mask", torch.uint8),
+                         (scratch_pos, "scratch_pos", torch.int32)):
+            _need(t, dt, n)
+            if t.shape != (scratch.shape[2], scratch.shape[4]) or not t.is_contiguous():
+                raise ValueError(f"{n} must be a contiguous [rows, scratch cap] tensor")
+        a.scratch_ids, a.scratch_mask, a.scratch_pos = (scratch_ids.data_ptr(),
+                                                        scratch_mask.data_ptr(),
+                                                        scratch_pos.data_ptr())
+    _check(lib.specdec_pool_gather(ctypes.byref(a), _stream(stream)), "specdec_pool_gather")
+
+
+def pool_append(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len, width,
+                accept_len, out_token, draft, status, in_place=False, stream=None):
+    """Append a verified batch back to its pool slots (see specdec.h)."""
+    a = _pool_args(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len,
+                   width, status, 0, in_place)
+    for name, t in (("accept_len", accept_len), ("out_token", out_token), ("draft", draft)):
+        _need(t, torch.int32, name)
+        setattr(a, name, t.data_ptr())
+    _check(lib.specdec_pool_append(ctypes.byref(a), _stream(stream)), "specdec_pool_append")

@@ -24,3 +24,10 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    """Build libspecdec.so once per session (a no-op when it is up to date)."""
+    from speculative_decoding_specdec_gb300 import _build
+    return _build.build()

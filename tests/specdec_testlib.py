@@ -1,0 +1,66 @@
+"""Side-by-side round runner for the GPU path and the CPU oracle (test infrastructure)."""
+import numpy as np
+import torch
+
+import oracle.specdec_oracle as O
+from speculative_decoding_specdec_gb300 import synth
+
+
+def eqspec_rounds(L, H, hd, kv_dtype, B, D, V, rounds, prompt_lo, prompt_hi, seed,
+                  copy_engine=0, alpha=0.6, logit_dtype=torch.float32, cap_extra=0,
+                  check_full_dst=True):
+    """Greedy verify + realign for ``rounds`` rounds with tagged K/V; every round is compared
+    with the oracle: accept lengths, tokens, lengths, width, ids, mask, position IDs, and the
+    whole destination cache (the oracle leaves pad columns as they were, and so must the
+    kernel).  Returns the per-round accept lengths."""
+    from speculative_decoding_specdec_gb300.engine import EqspecBatch
+    gen = synth.make_gen(seed)
+    n0 = synth.lengths_uniform(gen, B, prompt_lo, prompt_hi)
+    prompts = [torch.randint(0, V, (int(n),), generator=gen).tolist() for n in n0]
+    cap = int(n0.max()) + rounds * (D + 1) + D + 1 + cap_extra
+    eng = EqspecBatch(L, H, hd, kv_dtype, B, D, cap, rounds)
+    W = eng.start(prompts)
+    eng.kv[0].fill_(-3.0)
+    eng.kv[1].fill_(-5.0)
+    toks = [list(p) for p in prompts]
+    for b in range(B):
+        synth.write_tagged_columns(eng.cache, b, W - len(toks[b]), b,
+                                   list(range(len(toks[b]) - 1)), toks[b][:-1])
+    ids = eng.ids[0].cpu().numpy()
+    n = np.array([len(t) for t in toks])
+    history = []
+    for _ in range(rounds):
+        logits, draft = synth.greedy_round(gen, B, D, V, alpha, dtype=logit_dtype)
+        for b in range(B):
+            synth.write_tagged_columns(eng.cache, b, W - 1, b,
+                                       list(range(len(toks[b]) - 1, len(toks[b]) + D)),
+                                       [toks[b][-1]] + draft[b].tolist())
+        src = eng.cache.cpu().numpy()
+        dst_before = eng.kv[1 - eng.cur].cpu().numpy()
+        dd = draft.cuda()
+        eng.verify_greedy(logits.cuda(), dd)
+        eng.realign(dd, copy_engine=copy_engine)
+        torch.cuda.synchronize()
+        assert int(eng.status.item()) == 0
+        a, y = O.verify_greedy(logits.double().numpy(), draft.numpy())
+        kv, ids, mask, pos, n, W = O.realign(src, dst_before, n, W, a, y, draft.numpy(), ids, 0)
+        np.testing.assert_array_equal(eng.accept_len.cpu().numpy(), a)
+        np.testing.assert_array_equal(eng.out_token.cpu().numpy(), y)
+        assert int(eng.width.item()) == W
+        np.testing.assert_array_equal(eng.n_committed.cpu().numpy(), n)
+        np.testing.assert_array_equal(eng.ids[eng.cur].cpu().numpy(), ids)
+        np.testing.assert_array_equal(eng.mask[eng.cur].cpu().numpy(), mask)
+        np.testing.assert_array_equal(eng.pos[eng.cur].cpu().numpy(), pos)
+        assert O.check_invariants(eng.mask[eng.cur].cpu().numpy(), eng.pos[eng.cur].cpu().numpy(),
+                                  n, W) == []
+        got = eng.cache.cpu().numpy()
+        if check_full_dst:
+            np.testing.assert_array_equal(got, kv)
+        else:
+            for b in range(B):
+                lo = W - int(n[b])
+                np.testing.assert_array_equal(got[:, :, b, :, lo:W - 1], kv[:, :, b, :, lo:W - 1])
+        for b in range(B):
+            toks[b] += draft[b, :a[b]].tolist() + [int(y[b])]
+        history.append(a)
+    return history

@@ -1,0 +1,106 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol, the ctypes structs
+match the C layout, and host-side validation returns the documented codes (no kernel runs)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specdec.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\s*\*)\s+(specdec_\w+)\s*\(", text, re.M)))
+
+
+def test_every_declared_symbol_is_exported():
+    import speculative_decoding_specdec_gb300.specdec as sd
+    names = declared_functions()
+    assert "specdec_realign" in names and "specdec_verify_sample" in names
+    missing = [n for n in names if not hasattr(sd.lib, n)]
+    assert missing == []
+    assert sd.version() == 100
+
+
+def test_status_strings():
+    import speculative_decoding_specdec_gb300.specdec as sd
+    assert sd.status_string(0) == "ok"
+    assert "capacity" in sd.status_string(4)
+    assert sd.status_string(99) == "unknown status"
+
+
+STRUCT_PROBE = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "specdec.h"
+#define F(T, f) printf(#T "." #f " %zu\n", offsetof(T, f));
+int main(void) {
+  printf("specdec_kv_view %zu\n", sizeof(specdec_kv_view));
+  printf("specdec_realign_args %zu\n", sizeof(specdec_realign_args));
+  printf("specdec_pool_args %zu\n", sizeof(specdec_pool_args));
+  %FIELDS%
+  return 0;
+}
+"""
+
+
+def test_ctypes_layout_matches_c(tmp_path):
+    import speculative_decoding_specdec_gb300.specdec as sd
+    structs = {"specdec_kv_view": sd.KvView, "specdec_realign_args": sd.RealignArgs,
+               "specdec_pool_args": sd.PoolArgs}
+    fields = "\n".join(f"F({cn}, {f})" for cn, py in structs.items() for f, _ in py._fields_)
+    src = tmp_path / "probe.c"
+    src.write_text(STRUCT_PROBE.replace("%FIELDS%", fields))
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)],
+                   check=True)
+    out = dict(line.rsplit(" ", 1) for line in
+               subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+               if line)
+    for cn, py in structs.items():
+        assert int(out[cn]) == ctypes.sizeof(py), cn
+        for f, _ in py._fields_:
+            assert int(out[f"{cn}.{f}"]) == getattr(py, f).offset, (cn, f)
+
+
+def test_host_validation_codes():
+    import speculative_decoding_specdec_gb300.specdec as sd
+    L = sd.lib
+    # verify_greedy: empty batch is a no-op; bad sizes and NULL pointers are caught on the host
+    assert L.specdec_verify_greedy(None, sd.BF16, 0, 4, 100, 100, None, None, None, None, None) == sd.OK
+    assert L.specdec_verify_greedy(None, sd.BF16, 1, 4, 100, 100, None, None, None, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_verify_greedy(None, sd.BF16, 1, 0, 100, 100, None, None, None, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_verify_greedy(None, sd.BF16, 1, 32, 100, 100, None, None, None, None, None) == sd.ERR_UNSUPPORTED
+    assert L.specdec_verify_greedy(None, 7, 1, 4, 100, 100, None, None, None, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_verify_greedy(None, sd.F32, 1, 4, 100, 99, None, None, None, None, None) == sd.ERR_INVALID_ARG
+    # realign: NULL args, empty batch, bad views
+    assert L.specdec_realign(None, None) == sd.ERR_INVALID_ARG
+    a = sd.RealignArgs()
+    a.B, a.D = 0, 4
+    assert L.specdec_realign(ctypes.byref(a), None) == sd.OK
+    a.B = 2
+    assert L.specdec_realign(ctypes.byref(a), None) == sd.ERR_INVALID_ARG     # NULL cache base
+    a.src = sd.KvView(16, 64, 32, 16, 8, sd.BF16, 1, 2, 1, 4, 2)            # head_dim*2 = 8 bytes
+    a.dst = sd.KvView(4096, 64, 32, 16, 8, sd.BF16, 1, 2, 1, 4, 2)
+    assert L.specdec_realign(ctypes.byref(a), None) == sd.ERR_UNSUPPORTED
+    a.D = 40
+    assert L.specdec_realign(ctypes.byref(a), None) == sd.ERR_UNSUPPORTED
+    # grouping
+    assert L.specdec_group_by_length(None, -1, 8, 10, None, None, None, None, None, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_group_by_length(None, 5000, 8, 10, None, None, None, None, None, None, None) == sd.ERR_UNSUPPORTED
+    assert L.specdec_group_by_length(None, 4, 8, 20000, None, None, None, None, None, None, None) == sd.ERR_UNSUPPORTED
+    assert L.specdec_group_by_length(None, 4, 0, 10, None, None, None, None, None, None, None) == sd.ERR_INVALID_ARG
+    # pool moves
+    assert L.specdec_pool_gather(None, None) == sd.ERR_INVALID_ARG
+    p = sd.PoolArgs()
+    assert L.specdec_pool_append(ctypes.byref(p), None) == sd.ERR_INVALID_ARG
+
+
+def test_binding_raises_on_host_error():
+    import speculative_decoding_specdec_gb300.specdec as sd
+    with pytest.raises(sd.SpecdecError) as e:
+        sd._check(sd.ERR_CAPACITY, "x")
+    assert e.value.code == sd.ERR_CAPACITY

@@ -1,0 +1,162 @@
+"""Pool gather / append (EXSPEC mixed leftovers) on the GPU against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle.specdec_oracle as O
+from speculative_decoding_specdec_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _pool(S, cap, L, H, hd, V, gen, lo, hi):
+    dev = "cuda"
+    arena = torch.full((L, 2, 1, H, S * cap, hd), -9.0, device=dev)
+    n = synth.lengths_uniform(gen, S, lo, hi)
+    toks = [torch.randint(0, V, (int(n[s]),), generator=gen).tolist() for s in range(S)]
+    for s in range(S):
+        synth.write_tagged_columns(arena, 0, s * cap, s, list(range(len(toks[s]) - 1)),
+                                   toks[s][:-1])
+    pool_ids = torch.zeros(S, cap, dtype=torch.int32)
+    for s in range(S):
+        pool_ids[s, :len(toks[s])] = torch.tensor(toks[s], dtype=torch.int32)
+    i32 = lambda x: torch.as_tensor(x, dtype=torch.int32, device=dev)  # noqa: E731
+    return dict(arena=arena, slot_col=i32(np.arange(S) * cap), slot_cap=i32([cap] * S),
+                slot_len=i32(n.numpy()), pool_ids=pool_ids.to(dev), toks=toks)
+
+
+def test_gather_append_rounds_match_oracle():
+    import speculative_decoding_specdec_gb300.specdec as sd
+    gen = synth.make_gen(21)
+    S, cap, L, H, hd, D, V, R = 12, 80, 2, 3, 64, 4, 50, 5
+    P = _pool(S, cap, L, H, hd, V, gen, 2, 40)
+    dev = "cuda"
+    Sc = 40 + 8 * (D + 1) + D + 1
+    scratch = torch.full((L, 2, R, H, Sc, hd), 5.0, device=dev)
+    s_ids = torch.zeros(R, Sc, dtype=torch.int32, device=dev)
+    s_mask = torch.zeros(R, Sc, dtype=torch.uint8, device=dev)
+    s_pos = torch.zeros(R, Sc, dtype=torch.int32, device=dev)
+    blen = torch.zeros(R, dtype=torch.int32, device=dev)
+    width = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    rng = np.random.default_rng(2)
+    for _ in range(6):
+        k = int(rng.integers(1, R + 1))
+        rows_np = rng.choice(S, size=k, replace=False).astype(np.int32)
+        rows = torch.as_tensor(rows_np, device=dev)
+        ar0 = P["arena"][:, :, 0].cpu().numpy()
+        n_np = P["slot_len"].cpu().numpy()
+        ids_np = P["pool_ids"].cpu().numpy()
+        sc0 = scratch.cpu().numpy()
+        sd.pool_gather(P["arena"], scratch, rows, D, P["slot_col"], P["slot_cap"], P["slot_len"],
+                       P["pool_ids"], blen, width, st, s_ids, s_mask, s_pos)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        exp_sc, W, eids, emask, epos = O.pool_gather(ar0, np.arange(S) * cap, n_np, rows_np.tolist(),
+                                                   sc0, 0, ids_np)
+        assert int(width.item()) == W
+        np.testing.assert_array_equal(blen.cpu().numpy()[:k], n_np[rows_np])
+        np.testing.assert_array_equal(scratch.cpu().numpy(), exp_sc)
+        np.testing.assert_array_equal(s_ids.cpu().numpy()[:k], eids)
+        np.testing.assert_array_equal(s_mask.cpu().numpy()[:k], emask)
+        np.testing.assert_array_equal(s_pos.cpu().numpy()[:k], epos)
+        # synthetic verification pass on the padded batch, then greedy verification
+        logits, draft = synth.greedy_round(gen, k, D, V, 0.6, dtype=torch.float32)
+        for i, s in enumerate(rows_np):
+            t = P["toks"][s]
+            synth.write_tagged_columns(scratch, i, W - 1, int(s), list(range(len(t) - 1, len(t) + D)),
+                                       [t[-1]] + draft[i].tolist())
+        a, y = O.verify_greedy(logits.double().numpy(), draft.numpy())
+        ar1 = P["arena"][:, :, 0].cpu().numpy()
+        sc1 = scratch.cpu().numpy()
+        ga = torch.as_tensor(a, device=dev)
+        gy = torch.as_tensor(y, device=dev)
+        sd.pool_append(P["arena"], scratch, rows, D, P["slot_col"], P["slot_cap"], P["slot_len"],
+                       P["pool_ids"], blen, width, ga, gy, draft.to(dev), st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        exp_ar, exp_len, exp_ids = O.pool_append(ar1, np.arange(S) * cap, n_np, rows_np.tolist(),
+                                                 sc1, W, a, y, draft.numpy(), ids_np)
+        np.testing.assert_array_equal(P["arena"][:, :, 0].cpu().numpy(), exp_ar)
+        np.testing.assert_array_equal(P["slot_len"].cpu().numpy(), exp_len)
+        np.testing.assert_array_equal(P["pool_ids"].cpu().numpy(), exp_ids)
+        for i, s in enumerate(rows_np):
+            P["toks"][s] = P["toks"][s] + draft[i, :a[i]].tolist() + [int(y[i])]
+    # every slot equals a from-scratch rebuild of its sequence
+    got = P["arena"][:, :, 0].cpu().numpy()
+    for s in range(S):
+        t = P["toks"][s]
+        ref = torch.zeros(L, 2, 1, H, len(t) - 1, hd)
+        synth.write_tagged_columns(ref, 0, 0, s, list(range(len(t) - 1)), t[:-1])
+        np.testing.assert_array_equal(got[:, :, :, s * cap:s * cap + len(t) - 1], ref[:, :, 0].numpy())
+
+
+def test_in_place_uniform_batch():
+    import speculative_decoding_specdec_gb300.specdec as sd
+    gen = synth.make_gen(22)
+    S, cap, L, H, hd, D, V = 6, 60, 1, 2, 32, 3, 40
+    P = _pool(S, cap, L, H, hd, V, gen, 9, 9)          # all length 9
+    dev = "cuda"
+    scratch = torch.zeros(L, 2, 4, H, 16, hd, device=dev)
+    blen = torch.zeros(4, dtype=torch.int32, device=dev)
+    width = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    rows_np = np.array([4, 1, 2, 5], dtype=np.int32)
+    rows = torch.as_tensor(rows_np, device=dev)
+    sd.pool_gather(P["arena"], scratch, rows, D, P["slot_col"], P["slot_cap"], P["slot_len"],
+                   P["pool_ids"], blen, width, st, in_place=True)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(width.item()) == 9 and (blen == 9).all()
+    assert (scratch == 0).all()                         # nothing was gathered
+    logits, draft = synth.greedy_round(gen, 4, D, V, 0.6, dtype=torch.float32)
+    for i, s in enumerate(rows_np):                     # the pass writes into the slots
+        t = P["toks"][s]
+        synth.write_tagged_columns(P["arena"], 0, int(s) * cap + 8, int(s), list(range(8, 9 + D)),
+                                   [t[-1]] + draft[i].tolist())
+    a, y = O.verify_greedy(logits.double().numpy(), draft.numpy())
+    ar1 = P["arena"][:, :, 0].cpu().numpy()
+    n_np = P["slot_len"].cpu().numpy()
+    ids_np = P["pool_ids"].cpu().numpy()
+    sd.pool_append(P["arena"], scratch, rows, D, P["slot_col"], P["slot_cap"], P["slot_len"],
+                   P["pool_ids"], blen, width, torch.as_tensor(a, device=dev),
+                   torch.as_tensor(y, device=dev), draft.to(dev), st, in_place=True)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # expected: the slot columns stay where the pass wrote them; lengths and ids advance
+    fake = np.zeros((L, 2, 4, H, 9 + D, hd), np.float32)
+    for i, s in enumerate(rows_np):
+        fake[:, :, i, :, 8:9 + D] = ar1[:, :, :, s * cap + 8:s * cap + 9 + D]
+    exp_ar, exp_len, exp_ids = O.pool_append(ar1, np.arange(S) * cap, n_np, rows_np.tolist(), fake,
+                                             9, a, y, draft.numpy(), ids_np)
+    np.testing.assert_array_equal(P["arena"][:, :, 0].cpu().numpy(), exp_ar)
+    np.testing.assert_array_equal(P["slot_len"].cpu().numpy(), exp_len)
+    np.testing.assert_array_equal(P["pool_ids"].cpu().numpy(), exp_ids)
+
+
+def test_capacity_and_range_errors():
+    import speculative_decoding_specdec_gb300.specdec as sd
+    gen = synth.make_gen(23)
+    P = _pool(3, 20, 1, 1, 16, 30, gen, 15, 18)
+    dev = "cuda"
+    scratch = torch.zeros(1, 2, 3, 1, 12, 16, device=dev)    # too narrow for W + D
+    s_ids = torch.zeros(3, 12, dtype=torch.int32, device=dev)
+    s_mask = torch.zeros(3, 12, dtype=torch.uint8, device=dev)
+    s_pos = torch.zeros(3, 12, dtype=torch.int32, device=dev)
+    blen = torch.zeros(3, dtype=torch.int32, device=dev)
+    width = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    rows = torch.tensor([0, 1, 2], dtype=torch.int32, device=dev)
+    sd.pool_gather(P["arena"], scratch, rows, 2, P["slot_col"], P["slot_cap"], P["slot_len"],
+                   P["pool_ids"], blen, width, st, s_ids, s_mask, s_pos)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 4 and (scratch == 0).all() and int(width.item()) == 0
+    st.zero_()
+    blen.fill_(5)
+    width.fill_(6)
+    bad = torch.tensor([0, 3, 1], dtype=torch.int32, device=dev)   # 3 > D = 2
+    before = P["slot_len"].clone()
+    sd.pool_append(P["arena"], scratch, rows, 2, P["slot_col"], P["slot_cap"], P["slot_len"],
+                   P["pool_ids"], blen, width, bad, bad, torch.zeros(3, 2, dtype=torch.int32, device=dev),
+                   st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5 and torch.equal(before, P["slot_len"])
