@@ -350,7 +350,7 @@ def oracle_round_sampler(wname, seed=0, layers_sample=2):
     return w, Ls, one_round
 
 
-def time_oracle(wname, budget_s=15.0, max_rounds=None):
+def time_oracle(wname, budget_s=15.0, max_rounds=60):
     """Rounds/s of the oracle on a bounded sample (verify timed whole, realign on a layer sample
     scaled to all layers)."""
     w, Ls, one_round = oracle_round_sampler(wname)
@@ -360,7 +360,7 @@ def time_oracle(wname, budget_s=15.0, max_rounds=None):
         t_verify, t_realign = one_round()
         total += t_verify + t_realign * (w.layers / Ls)
         rounds += 1
-        if time.perf_counter() - start > budget_s or (max_rounds and rounds >= max_rounds):
+        if time.perf_counter() - start > budget_s or rounds >= max_rounds:
             break
     return rounds / total, rounds, Ls, w
 
@@ -369,7 +369,7 @@ def run_reference(args, rank, ws):
     if rank != 0:
         return None
     rps, rounds, Ls, w = time_oracle(args.workload, budget_s=max(10.0, 2.0 * args.steps),
-                                     max_rounds=args.warmup + args.steps)
+                                     max_rounds=min(60, args.warmup + args.steps))
     sample = (f"{rounds} rounds of {w.name}: verification of all {w.B} rows, realignment of "
               f"{Ls} of {w.layers} layers scaled x{w.layers / Ls:g}")
     return {"value": rps, "cpu_baseline": {"value": rps, "unit": "rounds/s", "cores": 1,

@@ -6,6 +6,11 @@ import oracle.specdec_oracle as O
 from speculative_decoding_specdec_gb300 import synth
 
 
+def host_bits(t):
+    """Host copy of a cache tensor; bf16 as its int16 bit patterns (values are only moved)."""
+    return (t.view(torch.int16) if t.dtype == torch.bfloat16 else t).cpu().numpy()
+
+
 def eqspec_rounds(L, H, hd, kv_dtype, B, D, V, rounds, prompt_lo, prompt_hi, seed,
                   copy_engine=0, alpha=0.6, logit_dtype=torch.float32, cap_extra=0,
                   check_full_dst=True):
@@ -35,8 +40,8 @@ def eqspec_rounds(L, H, hd, kv_dtype, B, D, V, rounds, prompt_lo, prompt_hi, see
             synth.write_tagged_columns(eng.cache, b, W - 1, b,
                                        list(range(len(toks[b]) - 1, len(toks[b]) + D)),
                                        [toks[b][-1]] + draft[b].tolist())
-        src = eng.cache.cpu().numpy()
-        dst_before = eng.kv[1 - eng.cur].cpu().numpy()
+        src = host_bits(eng.cache)
+        dst_before = host_bits(eng.kv[1 - eng.cur])
         dd = draft.cuda()
         eng.verify_greedy(logits.cuda(), dd)
         eng.realign(dd, copy_engine=copy_engine)
@@ -53,7 +58,7 @@ def eqspec_rounds(L, H, hd, kv_dtype, B, D, V, rounds, prompt_lo, prompt_hi, see
         np.testing.assert_array_equal(eng.pos[eng.cur].cpu().numpy(), pos)
         assert O.check_invariants(eng.mask[eng.cur].cpu().numpy(), eng.pos[eng.cur].cpu().numpy(),
                                   n, W) == []
-        got = eng.cache.cpu().numpy()
+        got = host_bits(eng.cache)
         if check_full_dst:
             np.testing.assert_array_equal(got, kv)
         else:
