@@ -38,6 +38,8 @@ def parse():
     p.add_argument("--impl", default="specdec", choices=["specdec", "reference"])
     p.add_argument("--copy-engine", type=int, default=0)
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--layers", type=int, default=0,
+                   help="override the workload's layer count (smaller cache, e.g. for ncu)")
     return p.parse_args()
 
 
@@ -104,7 +106,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -152,13 +154,20 @@ def measured_peaks():
 
 # ------------------------------------------------------------------------------ GPU arm
 
+def workload(args):
+    import dataclasses
+    from speculative_decoding_specdec_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    return dataclasses.replace(w, layers=args.layers) if args.layers else w
+
+
 def run_specdec(args, rank, ws, local):
     import numpy as np
     import torch
     from speculative_decoding_specdec_gb300 import synth
     from speculative_decoding_specdec_gb300.engine import EqspecBatch
 
-    w = synth.WORKLOADS[args.workload]
+    w = workload(args)
     if w.mode == "pool":
         raise SystemExit("the pool workload is benchmarked by its own script section (not yet)")
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -381,8 +390,7 @@ def run_reference(args, rank, ws):
 def main():
     args = parse()
     rank, ws, local = dist_setup(args.gpus)
-    from speculative_decoding_specdec_gb300 import synth
-    w = synth.WORKLOADS[args.workload]
+    w = workload(args)
     config = {"workload": f"{w.name}: L={w.layers} KV heads={w.heads} head_dim={w.head_dim} "
                           f"B={w.B} D={w.D} V={w.V} {w.mode} verify",
               "B": w.B, "D": w.D, "V": w.V, "layers": w.layers, "kv_heads": w.heads,
