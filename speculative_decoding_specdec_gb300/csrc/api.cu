@@ -20,6 +20,39 @@ int sm_count() {
   return cached[dev];
 }
 
+int cluster_for_one_wave(const void* kernel, int rows, int c_min, int c_max, int threads,
+                         size_t smem, int* cache) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return c_min;
+  int* active = cache + 17 * dev;
+  for (int c = c_max; c > c_min; --c) {
+    if (active[c] == 0) {
+      int n = -1;
+      if (c > 8 && cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                        1) != cudaSuccess) {
+        n = -1;
+      } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = c;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(c);
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = -1;
+      }
+      (void)cudaGetLastError();
+      active[c] = n == 0 ? -1 : n;
+    }
+    if (active[c] >= rows) return c;
+  }
+  return c_min;
+}
+
 int map_cuda_error(cudaError_t e) {
   if (e == cudaSuccess) return SPECDEC_OK;
   (void)cudaGetLastError();  // clear a non-sticky launch error so later calls start clean

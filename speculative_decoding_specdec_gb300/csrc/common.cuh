@@ -87,6 +87,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// As mbar_wait_bounded, but each poll lets the thread sleep until the phase completes or about
+// `sleep_ns` pass (the try_wait suspend-time hint), so waiting warps do not spin on issue slots.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t max_tries,
+                                                uint32_t sleep_ns) {
+  const uint32_t a = smem_addr(bar);
+  for (uint32_t it = 0; it < max_tries; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done) : "r"(a), "r"(parity), "r"(sleep_ns) : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
 // ----------------------------------------------------------------------------------- bulk copy
 
 // global -> shared (this CTA), completion counted on `bar` in bytes.
@@ -120,6 +137,13 @@ __device__ __forceinline__ void bulk_wait_all() {
 // ----------------------------------------------------------------------------------- host
 
 int sm_count();                  // multiprocessors of the current device (cached per device)
+
+// Cluster size for a grid of `rows` clusters of one kernel: the largest C in [c_min, c_max]
+// (c_max <= 16) for which all `rows` clusters of C CTAs (threads each, smem dynamic bytes) can
+// be resident at once, by cudaOccupancyMaxActiveClusters; c_min when none can.  Results are
+// cached per device in `cache` (17 ints per device, 0 = not yet queried).
+int cluster_for_one_wave(const void* kernel, int rows, int c_min, int c_max, int threads,
+                         size_t smem, int* cache);
 int map_cuda_error(cudaError_t); // SPECDEC_OK or SPECDEC_ERR_CUDA (clears non-sticky errors)
 
 inline int elem_size(int dtype) { return dtype == SPECDEC_F32 ? 4 : dtype == SPECDEC_BF16 ? 2 : 0; }

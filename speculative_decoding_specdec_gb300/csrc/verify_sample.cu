@@ -7,72 +7,141 @@
 //   "Draft Possible Tokens, Then Verify Them Together": left to right, the first rejection ends
 //   the cycle, and a fully accepted draft earns a bonus token from the distribution after it.
 //
-// GB300 mapping.  One thread-block cluster of C CTAs per batch row b; CTA c owns the vocabulary
+// GB300 mapping.  One thread-block cluster of C CTAs per batch row b (C <= 16, chosen so the grid
+// fills one wave of resident CTAs); CTA c owns the vocabulary
 // slice [c*slice, (c+1)*slice).
-//  Phase 1  every CTA streams its slice of the 2D+1 score rows (D+1 target, D draft) once with
-//           16-byte loads and keeps a per-lane online (max, sum of exp2((x - max) * log2(e)/T));
-//           warps and the CTA combine partials, the CTA's in fp64.
-//  Phase 2  after a cluster barrier every CTA combines the C partials of every row through
-//           distributed shared memory (same order everywhere, so every CTA gets the same bits),
-//           and warp 0 computes p_j(d)/q_j(d) for each draft in fp64 from the two scores of d and
-//           the normalisers, accepts while u < p/q, and finds the first rejection a with a ballot.
-//  Phase 3  each CTA re-reads only row a of both models (L2-warm) or row D of the target (bonus),
-//           keeps the residual max(0, p - q) (or p_D) of its slice in shared memory, and takes a
-//           block prefix sum.  A second cluster barrier exchanges slice totals; the CTA whose
-//           cumulative range holds t = u[b][D] * R finds the token with its block scan.
+//  Phase 1  a producer thread streams the slice of the 2D+1 score rows (D+1 target, D draft)
+//           through a 192 KB shared-memory ring in 32 KB cp.async.bulk copies (rows stored back
+//           to back are read as one contiguous range per CTA; its idle lanes meanwhile fetch
+//           the drafts, uniforms and the two scores of every draft); 16 consumer warps keep,
+//           per thread and row, a sum s of 2^(x*c2 - o) with c2 = log2(e)/T and an INTEGER offset
+//           o.  A new maximum more than 64 binary orders above o moves o; rescaling by 2^(old-new)
+//           is then exact, so per score element the work is one FFMA, one ex2.approx and one add.
+//           Warps, the CTA (fp64) and the cluster (fp64, through distributed shared memory, one
+//           per-row warp reduction) merge (o, s) pairs with the same exact scalings.
+//  Phase 2  warp 0 of every CTA computes p_j(d)/q_j(d) in fp64 from the two scores of d and the
+//           normalisers, accepts while u < p/q, and finds the first rejection a with a ballot.
+//  Phase 3  each CTA stages its slice of row a of both models (or row D of the target for the
+//           bonus) in the ring's space with two bulk copies, recomputes the residual
+//           max(0, p - q) (or p_D) from it where needed, and takes a block prefix sum.  A cluster
+//           barrier exchanges slice totals; the CTA whose cumulative range holds t = u[b][D] * R
+//           finds the token with its block scan.
 // No global scratch and no atomics; the score rows are read once (plus the one re-read row).
 #include <cooperative_groups.h>
 
+#include <algorithm>
 #include <cmath>
 
-#include "common.cuh"
+#include "stream.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace specdec {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kVecPerLane = 4;
+constexpr int kWarps = 16;                    // consumer warps
+constexpr int kAllWarps = kWarps + 1;         // plus the producer warp
+constexpr int kThreads = kAllWarps * 32;
+constexpr int kConsumers = kWarps * 32;
+constexpr int kRingBytes = 192 * 1024;  // one CTA per SM, six 32 KB stages
+constexpr int kChunkBytes = 32768;      // bytes per bulk copy
 constexpr int kMaxQ = 2 * SPECDEC_MAX_DRAFT + 1;  // score rows per batch row
-constexpr int kMaxSliceBytes = 160 * 1024;        // shared-memory residual slice
 constexpr float kLog2e = 1.4426950408889634f;     // log2(e)
 constexpr float kNegInf = -INFINITY;
+constexpr float kOffsetNone = -1e30f;             // offset of an empty sum
+constexpr float kRescale = 18446744073709551616.f;  // 2^64: a vector sum above it moves o
 
 // Slice length: ceil(V / C) rounded up to whole 16-byte vectors.
 __host__ __device__ constexpr int V_ceil(int V, int C, int vn) {
   return ((V + C - 1) / C + vn - 1) / vn * vn;
 }
 
-// Merge (om, os) into (m, s): sums are relative to their maxima; -inf max means an empty sum.
-__device__ __forceinline__ void merge(float& m, float& s, float om, float os, float c2) {
-  const float M = fmaxf(m, om);
-  const float f1 = (m == kNegInf) ? 0.f : exp2f((m - M) * c2);
-  const float f2 = (om == kNegInf) ? 0.f : exp2f((om - M) * c2);
-  s = s * f1 + os * f2;
-  m = M;
+// 2^x by the PTX instruction ex2.approx.ftz.f32 (relative error within 2^-22 by the PTX ISA;
+// results below the normal range are flushed to zero, which only drops negligible terms).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-__device__ __forceinline__ void warp_merge(float& m, float& s, float c2) {
+// Exact 2^k for an integer-valued k <= 0 (offset differences), built from the IEEE-754 fields.
+__device__ __forceinline__ float pow2f(float k) {
+  if (!(k >= -126.f)) return 0.f;
+  return __int_as_float((static_cast<int>(k) + 127) << 23);
+}
+__device__ __forceinline__ double pow2d(float k) {
+  if (!(k >= -1022.f)) return 0.0;
+  return __longlong_as_double(static_cast<long long>(static_cast<int>(k) + 1023) << 52);
+}
+
+// Merge (oo, os) into (o, s): both sums are relative to their integer offsets.
+__device__ __forceinline__ void merge(float& o, float& s, float oo, float os) {
+  const float M = fmaxf(o, oo);
+  s = s * pow2f(o - M) + os * pow2f(oo - M);
+  o = M;
+}
+
+__device__ __forceinline__ void warp_merge(float& o, float& s) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float om = __shfl_xor_sync(0xffffffffu, m, o);
-    const float os = __shfl_xor_sync(0xffffffffu, s, o);
-    merge(m, s, om, os, c2);
+  for (int k = 16; k > 0; k >>= 1) {
+    const float oo = __shfl_xor_sync(0xffffffffu, o, k);
+    const float os = __shfl_xor_sync(0xffffffffu, s, k);
+    merge(o, s, oo, os);
   }
 }
 
-__device__ __forceinline__ double warp_sum(double v) {
+// Fold N values into (o, s).
+template <int N>
+__device__ __forceinline__ void fold(const float* x, float c2, float& o, float& s) {
+  float v = 0.f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+  for (int i = 0; i < N; ++i) v += ex2(fmaf(x[i], c2, -o));
+  if (!(v <= kRescale)) {  // first finite values, a much larger maximum, or NaN/+inf
+    float mx = x[0];
+#pragma unroll
+    for (int i = 1; i < N; ++i) mx = fmaxf(mx, x[i]);
+    const float on = ceilf(mx * c2);
+    if (on > o) {
+      s *= pow2f(o - on);
+      o = on;
+    }
+    v = 0.f;
+#pragma unroll
+    for (int i = 0; i < N; ++i) v += ex2(fmaf(x[i], c2, -o));
+  }
+  s += v;
 }
 
-__device__ __forceinline__ float warp_fmax(float v) {
+// Fold four 16-byte vectors: independent tree sums (short dependency chains); if their total
+// would need a new offset, fall back to folding them one by one.
+template <typename T>
+__device__ __forceinline__ void fold4(const uint4* r, float c2, float& o, float& s) {
+  constexpr int VN = Vec<T>::N;
+  float t[4];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+  for (int k = 0; k < 4; ++k) {
+    float x[VN];
+    Vec<T>::unpack(r[k], x);
+    float e[VN];
+#pragma unroll
+    for (int i = 0; i < VN; ++i) e[i] = ex2(fmaf(x[i], c2, -o));
+#pragma unroll
+    for (int w = VN / 2; w > 0; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) e[i] += e[i + w];
+    t[k] = e[0];
+  }
+  const float v = (t[0] + t[1]) + (t[2] + t[3]);
+  if (v <= kRescale) {
+    s += v;
+  } else {  // first finite values, a much larger maximum, or NaN/+inf
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float x[VN];
+      Vec<T>::unpack(r[k], x);
+      fold<VN>(x, c2, o, s);
+    }
+  }
 }
 
 template <typename T, bool kVec>
@@ -109,19 +178,23 @@ struct SampleArgs {
 };
 
 template <typename T, bool kVec>
-__global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs A) {
-  extern __shared__ float rbuf[];  // residual of this CTA's slice
-  __shared__ float pm[kMaxQ][kWarps];
+__global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A) {
+  extern __shared__ __align__(128) char dyn[];  // phase 1: the ring; phase 3: two staged rows
+  __shared__ float po[kMaxQ][kWarps];
   __shared__ float ps[kMaxQ][kWarps];
-  __shared__ float cm[kMaxQ];   // this CTA's per-row partials, read by the whole cluster
+  __shared__ float co[kMaxQ];   // this CTA's per-row partials, read by the whole cluster
   __shared__ double cs[kMaxQ];
-  __shared__ float gm[kMaxQ];   // cluster-combined per-row max and normaliser
+  __shared__ float go[kMaxQ];   // cluster-combined per-row offset and normaliser
   __shared__ double gs[kMaxQ];
   __shared__ float incl[kThreads];
-  __shared__ float wtot[kWarps];
+  __shared__ float wtot[32];
   __shared__ double slice_sum[2];  // this CTA's residual total (second slot: fallback to p)
   __shared__ double s_R, s_P;
-  __shared__ int s_a, s_bad, s_found, s_y, s_last;
+  __shared__ int s_a, s_bad, s_found, s_y, s_last, s_fail;
+  __shared__ __align__(8) uint64_t full[kMaxRingStages], empty[kMaxRingStages], pbar;
+  __shared__ StreamPlan plan;
+  __shared__ int pre_d[SPECDEC_MAX_DRAFT];   // fetched while the slice streams
+  __shared__ float pre_u[SPECDEC_MAX_DRAFT + 1], pre_z[SPECDEC_MAX_DRAFT], pre_w[SPECDEC_MAX_DRAFT];
 
   cg::cluster_group cluster = cg::this_cluster();
   const T* tl = static_cast<const T*>(A.tl);
@@ -136,93 +209,170 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs A) {
   const int len = s1 - s0;
   const float c2 = kLog2e / A.temperature;
   constexpr int VN = Vec<T>::N;
+  const int body = kVec ? len / VN * VN : 0;  // vector-aligned part of the slice
+  // Rows stored back to back: phase 1 takes one contiguous range of the batch row's (2D+1)*V
+  // scores (target rows, then draft rows; large bulk copies); otherwise the vocabulary slice of
+  // every row, whose sub-vector tail is folded separately.
+  const bool contiguous = kVec && A.rs == V && V % VN == 0;
+  const int tail_from = contiguous ? s1 : s0 + body;
 
   auto row_ptr = [&](int q) -> const T* {  // q <= D: target row q; q > D: draft row q-D-1
     return q <= D ? tl + (static_cast<long long>(b) * (D + 1) + q) * A.rs
                   : dl + (static_cast<long long>(b) * D + (q - D - 1)) * A.rs;
   };
 
+  // Draft tokens, uniforms and the two scores of each draft: fetched by the producer warp's idle
+  // lanes 1..31 while the slice streams (item j = lane - 1, lane + 30, ...; D+1 uniforms).
+  auto prefetch = [&](int j) {
+    if (j <= D) pre_u[j] = A.uniforms[static_cast<long long>(b) * (D + 1) + j];
+    if (j < D) {
+      const int d = A.draft[static_cast<long long>(b) * D + j];
+      pre_d[j] = d;
+      if (d >= 0 && d < V) {
+        pre_z[j] = Vec<T>::scalar(row_ptr(j) + d);
+        pre_w[j] = Vec<T>::scalar(row_ptr(D + 1 + j) + d);
+      }
+    }
+  };
+
   for (int k = tid; k < kMaxQ * kWarps; k += kThreads) {
-    (&pm[0][0])[k] = kNegInf;
+    (&po[0][0])[k] = kOffsetNone;
     (&ps[0][0])[k] = 0.f;
   }
-  if (tid == 0) { s_bad = 0; s_found = 0; s_last = -1; }
+  if (tid == 0) {
+    s_bad = 0;
+    s_found = 0;
+    s_last = -1;
+    s_fail = 0;
+    for (int k = 0; k < kMaxRingStages; ++k) {
+      mbar_init(&full[k], 1);
+      mbar_init(&empty[k], kWarps);
+    }
+    mbar_init(&pbar, 1);
+    fence_mbar_init();
+    plan.V = V;
+    plan.esize = static_cast<int>(sizeof(T));
+    plan.nblk = 0;
+    if (contiguous) {
+      const long long nt = static_cast<long long>(D + 1) * V;  // target scores of this row
+      const long long units = (nt + static_cast<long long>(D) * V) / VN;
+      const long long e0 = units * rank / C * VN, e1 = units * (rank + 1) / C * VN;
+      if (e0 < nt) {  // the target part of the range
+        const long long hi = min(e1, nt);
+        plan.blk[plan.nblk++] = StreamBlock{reinterpret_cast<const char*>(row_ptr(0) + e0),
+                                            static_cast<int>(hi - e0), static_cast<int>(e0 / V),
+                                            static_cast<int>(e0 % V)};
+      }
+      if (e1 > nt) {  // the draft part
+        const long long lo = max(e0, nt) - nt, hi = e1 - nt;
+        plan.blk[plan.nblk++] = StreamBlock{reinterpret_cast<const char*>(row_ptr(D + 1) + lo),
+                                            static_cast<int>(hi - lo),
+                                            D + 1 + static_cast<int>(lo / V),
+                                            static_cast<int>(lo % V)};
+      }
+    } else if (kVec && body > 0) {
+      for (int q = 0; q < Q; ++q)
+        plan.blk[plan.nblk++] =
+            StreamBlock{reinterpret_cast<const char*>(row_ptr(q) + s0), body, q, s0};
+    }
+    plan.finish(kChunkBytes / static_cast<int>(sizeof(T)), kRingBytes);
+  }
   __syncthreads();
 
   // ---------------------------------------------------------------- phase 1: normalisers
-  {
-    constexpr int UNIT = 32 * kVecPerLane * VN;
-    const int segs = (len + UNIT - 1) / UNIT;
-    const int units = Q * segs;
-    int cur = -1;
-    float m = kNegInf, s = 0.f;
-    for (int u = warp; u < units; u += kWarps) {  // warp-uniform trip count
-      const int q = u / segs, seg = u - q * segs;
-      if (q != cur) {
-        if (cur >= 0) {
-          warp_merge(m, s, c2);
-          if (lane == 0) { pm[cur][warp] = m; ps[cur][warp] = s; }
-        }
-        cur = q;
-        m = kNegInf;
-        s = 0.f;
+  if (kVec) {
+    if (warp == kWarps) {
+      if (lane == 0) {
+        if (!stream_produce(plan, dyn, full, empty)) s_fail = 1;
+      } else {
+        for (int j = lane - 1; j <= D; j += 31) prefetch(j);
       }
-      const T* row = row_ptr(q);
-      const int e0 = s0 + seg * UNIT;
-      uint4 buf[kVecPerLane];
+    } else {
+      int cur = -1;
+      float o = kOffsetNone, s = 0.f;
+      const bool ok = stream_consume(
+          plan, dyn, full, empty, [&](int q, int, int n, const char* stage) {  // row segment
+            if (q != cur) {
+              if (cur >= 0) {
+                warp_merge(o, s);
+                if (lane == 0) { po[cur][warp] = o; ps[cur][warp] = s; }
+              }
+              cur = q;
+              o = kOffsetNone;
+              s = 0.f;
+            }
+            const uint4* v4 = reinterpret_cast<const uint4*>(stage);
+            const int nv = n / VN;
+            int v = tid;
+            for (; v + 3 * kConsumers < nv; v += 4 * kConsumers) {
+              uint4 r[4];
 #pragma unroll
-      for (int k = 0; k < kVecPerLane; ++k)
-        load_row_slice<T, kVec>(row, e0 + (k * 32 + lane) * VN, s1, buf[k]);
-      float x[kVecPerLane][VN];
-      float mu = kNegInf;
-#pragma unroll
-      for (int k = 0; k < kVecPerLane; ++k) {
-        values<T, kVec>(row, e0 + (k * 32 + lane) * VN, s1, buf[k], x[k]);
-#pragma unroll
-        for (int i = 0; i < VN; ++i) mu = fmaxf(mu, x[k][i]);
-      }
-      if (mu > m) {  // raise the running maximum (rescale what was summed so far)
-        s = (m == kNegInf) ? 0.f : s * exp2f((m - mu) * c2);
-        m = mu;
-      }
-      if (m != kNegInf) {
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < kVecPerLane; ++k)
-#pragma unroll
-          for (int i = 0; i < VN; ++i) acc += exp2f((x[k][i] - m) * c2);
-        s += acc;
+              for (int k = 0; k < 4; ++k) r[k] = v4[v + k * kConsumers];
+              fold4<T>(r, c2, o, s);
+            }
+            for (; v < nv; v += kConsumers) {
+              float x[VN];
+              Vec<T>::unpack(v4[v], x);
+              fold<VN>(x, c2, o, s);
+            }
+          });
+      if (!ok && lane == 0) s_fail = 1;
+      if (cur >= 0) {
+        warp_merge(o, s);
+        if (lane == 0) { po[cur][warp] = o; ps[cur][warp] = s; }
       }
     }
-    if (cur >= 0) {
-      warp_merge(m, s, c2);
-      if (lane == 0) { pm[cur][warp] = m; ps[cur][warp] = s; }
+  } else if (warp == kWarps) {
+    if (lane >= 1)
+      for (int j = lane - 1; j <= D; j += 31) prefetch(j);
+  } else {  // rows not 16-byte aligned: plain loads
+    for (int q = 0; q < Q; ++q) {
+      const T* row = row_ptr(q);
+      float o = kOffsetNone, s = 0.f;
+      for (int e = s0 + tid; e < s1; e += kConsumers) {
+        const float x = Vec<T>::scalar(row + e);
+        fold<1>(&x, c2, o, s);
+      }
+      warp_merge(o, s);
+      if (lane == 0) { po[q][warp] = o; ps[q][warp] = s; }
     }
   }
   __syncthreads();
-  for (int q = warp; q < Q; q += kWarps) {  // CTA partial per row, in fp64
-    const float m = lane < kWarps ? pm[q][lane] : kNegInf;
-    const float s = lane < kWarps ? ps[q][lane] : 0.f;
-    const float M = warp_fmax(m);
-    const double f = (m == kNegInf) ? 0.0 : static_cast<double>(exp2f((m - M) * c2));
-    const double S = warp_sum(static_cast<double>(s) * f);
-    if (lane == 0) { cm[q] = M; cs[q] = S; }
+  if (s_fail && tid == 0) set_status(A.status, SPECDEC_ERR_TIMEOUT);
+  for (int q = warp; q < Q; q += kAllWarps) {  // CTA partial per row (fp64), plus the tail
+    float o = lane < kWarps ? po[q][lane] : kOffsetNone;
+    float s = lane < kWarps ? ps[q][lane] : 0.f;
+    if (lane == kWarps && kVec) {  // elements past the streamed body (fewer than one vector)
+      const T* row = row_ptr(q);
+      for (int e = tail_from; e < s1; ++e) {
+        const float x = Vec<T>::scalar(row + e);
+        fold<1>(&x, c2, o, s);
+      }
+    }
+    float M = o;
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, k));
+    double S = static_cast<double>(s) * pow2d(o - M);
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) S += __shfl_xor_sync(0xffffffffu, S, k);
+    if (lane == 0) { co[q] = M; cs[q] = S; }
   }
   cluster.sync();  // #1: every CTA's partials are final
 
   // ---------------------------------------------------------------- phase 2: decisions
-  if (warp < 2) {
-    const int q = warp * 32 + lane;
-    if (q < Q) {
-      float M = kNegInf;
-      for (int r = 0; r < C; ++r) M = fmaxf(M, cluster.map_shared_rank(cm, r)[q]);
-      double S = 0.0;
-      for (int r = 0; r < C; ++r) {
-        const float m = cluster.map_shared_rank(cm, r)[q];
-        const double s = cluster.map_shared_rank(cs, r)[q];
-        if (m != kNegInf) S += s * static_cast<double>(exp2f((m - M) * c2));
-      }
-      gm[q] = M;
+  // Every CTA combines the C partials of every row: a warp per row, lane r loading rank r's
+  // partial through distributed shared memory (C <= 16), then a warp reduction.
+  for (int q = warp; q < Q; q += kAllWarps) {
+    const float o = lane < C ? cluster.map_shared_rank(co, lane)[q] : kOffsetNone;
+    const double sp = lane < C ? cluster.map_shared_rank(cs, lane)[q] : 0.0;
+    float M = o;
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, k));
+    double S = sp * pow2d(o - M);
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) S += __shfl_xor_sync(0xffffffffu, S, k);
+    if (lane == 0) {
+      go[q] = M;
       gs[q] = S;
     }
   }
@@ -233,27 +383,29 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs A) {
       if (!(gs[q] > 0.0) || !isfinite(gs[q])) bad = true;  // NaN/+inf scores or an empty row
     bool accept = true;
     if (lane < D) {
-      const int d = A.draft[static_cast<long long>(b) * D + lane];
-      const float u = A.uniforms[static_cast<long long>(b) * (D + 1) + lane];
+      const int d = pre_d[lane];
+      const float u = pre_u[lane];
       if (!(u >= 0.f && u < 1.f)) bad = true;
       if (d < 0 || d >= V) {
         bad = true;
         accept = false;
       } else {
-        const double z = static_cast<double>(Vec<T>::scalar(row_ptr(lane) + d));
-        const double w = static_cast<double>(Vec<T>::scalar(row_ptr(D + 1 + lane) + d));
-        if (w == -INFINITY) {
+        const float z = pre_z[lane];
+        const float w = pre_w[lane];
+        if (w == kNegInf) {
           accept = true;  // q(d) = 0
         } else {
-          const double lr = (z - w - (static_cast<double>(gm[lane]) - gm[D + 1 + lane])) /
-                            static_cast<double>(A.temperature);
-          const double ratio = exp(lr) * (gs[D + 1 + lane] / gs[lane]);  // p(d) / q(d)
+          // p(d)/q(d) = 2^(z*c2 - o_p) / S_p  /  (2^(w*c2 - o_q) / S_q), in fp64
+          const double c2d = static_cast<double>(c2);
+          const double e = (static_cast<double>(z) - static_cast<double>(w)) * c2d -
+                           (static_cast<double>(go[lane]) - static_cast<double>(go[D + 1 + lane]));
+          const double ratio = exp2(e) * (gs[D + 1 + lane] / gs[lane]);
           accept = static_cast<double>(u) < ratio;
         }
       }
     }
     if (lane == 0) {
-      const float u = A.uniforms[static_cast<long long>(b) * (D + 1) + D];
+      const float u = pre_u[D];
       if (!(u >= 0.f && u < 1.f)) bad = true;
     }
     const unsigned rej = __ballot_sync(0xffffffffu, lane < D && !accept);
@@ -267,58 +419,94 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs A) {
   const int a = s_a;
 
   // ---------------------------------------------------------------- phase 3: residual draw
-  // rbuf[v - s0] = max(0, p_a(v) - q_a(v)) after a rejection, p_D(v) for the bonus.
-  auto fill = [&](bool use_p) {
-    const int rz = a;                 // target row a (a == D: the bonus row)
-    const int rq = D + 1 + a;         // draft row a (a < D only)
-    const T* zrow = row_ptr(rz);
-    const float Mz = gm[rz];
-    const float iz = static_cast<float>(1.0 / gs[rz]);
-    const bool resid = (a < D) && !use_p;
-    const T* wrow = resid ? row_ptr(rq) : zrow;
-    const float Mw = resid ? gm[rq] : 0.f;
-    const float iw = resid ? static_cast<float>(1.0 / gs[rq]) : 0.f;
-    for (int e = s0 + tid * VN; e < s1; e += kThreads * VN) {
-      uint4 bz = make_uint4(0, 0, 0, 0), bw = make_uint4(0, 0, 0, 0);
-      load_row_slice<T, kVec>(zrow, e, s1, bz);
-      if (resid) load_row_slice<T, kVec>(wrow, e, s1, bw);
-      float xz[VN], xw[VN];
-      values<T, kVec>(zrow, e, s1, bz, xz);
-      if (resid) values<T, kVec>(wrow, e, s1, bw, xw);
+  // The slice of target row a (and draft row a after a rejection) is staged in shared memory
+  // (the ring's space, free again): one bulk copy each, the sub-vector tail by plain loads.  The
+  // residual r(i) = max(0, p_a - q_a) (or p, for the bonus and the p-fallback) is recomputed from
+  // the staged scores wherever it is needed, so it needs no storage of its own.
+  const bool resid = a < D;
+  const T* zrow = row_ptr(a);
+  const T* wrow = row_ptr(resid ? D + 1 + a : a);
+  const int stage_elems = ((len * static_cast<int>(sizeof(T)) + 127) / 128 * 128) /
+                          static_cast<int>(sizeof(T));
+  T* zs = reinterpret_cast<T*>(dyn);
+  T* ws = zs + stage_elems;
+  if (kVec && body > 0 && tid == kWarps * 32) {
+    const uint32_t bytes = static_cast<uint32_t>(body) * sizeof(T);
+    mbar_arrive_expect_tx(&pbar, resid ? 2 * bytes : bytes);
+    bulk_g2s(zs, zrow + s0, bytes, &pbar);
+    if (resid) bulk_g2s(ws, wrow + s0, bytes, &pbar);
+  }
+  for (int i = (kVec ? body : 0) + tid; i < len; i += kThreads) {  // tail / unaligned rows
+    zs[i] = zrow[s0 + i];
+    if (resid) ws[i] = wrow[s0 + i];
+  }
+  if (kVec && body > 0) {
+    const bool got = mbar_wait_sleep(&pbar, 0, kSleepTries, kSleepNs);
+    if (!got) s_fail = 1;
+  }
+  __syncthreads();
+  if (s_fail && tid == 0) set_status(A.status, SPECDEC_ERR_TIMEOUT);
+  const float oz = go[a];
+  const float iz = static_cast<float>(1.0 / gs[a]);
+  const float ow = resid ? go[D + 1 + a] : 0.f;
+  const float iw = resid ? static_cast<float>(1.0 / gs[D + 1 + a]) : 0.f;
+  bool use_p = !resid;
+  auto r_at = [&](int i) -> float {
+    const float p = ex2(fmaf(Vec<T>::scalar(zs + i), c2, -oz)) * iz;
+    if (use_p) return p;
+    return fmaxf(0.f, p - ex2(fmaf(Vec<T>::scalar(ws + i), c2, -ow)) * iw);
+  };
+  // The VN residual values of elements [i, i + VN) (i a multiple of VN, inside the slice).
+  auto r_vec = [&](int i, float* r) {
+    float z[VN];
+    Vec<T>::unpack(*reinterpret_cast<const uint4*>(zs + i), z);
 #pragma unroll
-      for (int i = 0; i < VN; ++i) {
-        if (e + i >= s1) break;
-        const float p = exp2f((xz[i] - Mz) * c2) * iz;
-        float r = p;
-        if (resid) r = fmaxf(0.f, p - exp2f((xw[i] - Mw) * c2) * iw);
-        rbuf[e + i - s0] = r;
-      }
+    for (int k = 0; k < VN; ++k) r[k] = ex2(fmaf(z[k], c2, -oz)) * iz;
+    if (!use_p) {
+      float w[VN];
+      Vec<T>::unpack(*reinterpret_cast<const uint4*>(ws + i), w);
+#pragma unroll
+      for (int k = 0; k < VN; ++k) r[k] = fmaxf(0.f, r[k] - ex2(fmaf(w[k], c2, -ow)) * iw);
     }
   };
-  // Block inclusive scan of per-thread contiguous chunk sums; returns the slice total.
-  const int K = (len + kThreads - 1) / kThreads;
+  // Block inclusive scan of per-thread contiguous chunk sums; returns the slice total.  Chunks
+  // start at multiples of VN so the staged scores are read 16 bytes at a time.
+  const int K = ((len + kThreads - 1) / kThreads + VN - 1) / VN * VN;
   const int c0 = min(len, tid * K), c1 = min(len, c0 + K);
+  const int cv = c0 + (c1 - c0) / VN * VN;  // end of this chunk's whole vectors
   auto scan = [&]() -> float {
-    __syncthreads();
-    float own = 0.f;
-    for (int i = c0; i < c1; ++i) own += rbuf[i];
+    float acc[VN];
+#pragma unroll
+    for (int k = 0; k < VN; ++k) acc[k] = 0.f;
+    for (int i = c0; i < cv; i += VN) {
+      float r[VN];
+      r_vec(i, r);
+#pragma unroll
+      for (int k = 0; k < VN; ++k) acc[k] += r[k];
+    }
+    for (int i = cv; i < c1; ++i) acc[0] += r_at(i);
+#pragma unroll
+    for (int w = VN / 2; w > 0; w >>= 1)
+#pragma unroll
+      for (int k = 0; k < w; ++k) acc[k] += acc[k + w];
+    const float own = acc[0];
     float v = own;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += t;
+    for (int k = 1; k < 32; k <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, v, k);
+      if (lane >= k) v += t;
     }
     if (lane == 31) wtot[warp] = v;
     __syncthreads();
     if (warp == 0) {
-      const float wv = lane < kWarps ? wtot[lane] : 0.f;
+      const float wv = lane < kAllWarps ? wtot[lane] : 0.f;
       float x = wv;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float t = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += t;
+      for (int k = 1; k < 32; k <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, x, k);
+        if (lane >= k) x += t;
       }
-      if (lane < kWarps) wtot[lane] = x - wv;  // exclusive warp offsets
+      if (lane < kAllWarps) wtot[lane] = x - wv;  // exclusive warp offsets
     }
     __syncthreads();
     incl[tid] = v + wtot[warp];
@@ -328,29 +516,31 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs A) {
   auto exchange = [&](int slot, float Rc) {  // R over the cluster and this CTA's offset
     if (tid == 0) slice_sum[slot] = static_cast<double>(Rc);
     cluster.sync();
-    if (tid == 0) {
-      double R = 0.0, P = 0.0;
+    if (warp == 0) {
+      const double x = lane < C ? cluster.map_shared_rank(slice_sum, lane)[slot] : 0.0;
+      double R = 0.0, P = 0.0;  // rank order in every CTA: P_c + Rc_c == P_{c+1} bit for bit
       for (int r = 0; r < C; ++r) {
-        const double x = cluster.map_shared_rank(slice_sum, r)[slot];
-        if (r < rank) P += x;
-        R += x;
+        const double xr = __shfl_sync(0xffffffffu, x, r);
+        if (r < rank) P += xr;
+        R += xr;
       }
-      s_R = R;
-      s_P = P;
+      if (lane == 0) {
+        s_R = R;
+        s_P = P;
+      }
     }
     __syncthreads();
   };
 
-  fill(false);
   float Rc = scan();
   exchange(0, Rc);  // #2
   if (!(s_R > 0.0) && a < D) {  // residual vanished (p == q): draw from p instead
-    fill(true);
+    use_p = true;
     Rc = scan();
     exchange(1, Rc);  // #2b
   }
   const double R = s_R, P = s_P;
-  const float u_draw = A.uniforms[static_cast<long long>(b) * (D + 1) + D];
+  const float u_draw = pre_u[D];
   const double t = static_cast<double>(u_draw) * R;
   const bool valid = (R > 0.0) && isfinite(R) && !s_bad;
   const bool owner = valid && Rc > 0.f && P <= t && t < P + static_cast<double>(Rc);
@@ -360,10 +550,22 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs A) {
     if (E <= tl_ && tl_ < incl[tid]) {
       float run = E;
       int y = -1, last = -1;
-      for (int i = c0; i < c1; ++i) {
-        if (rbuf[i] > 0.f) last = i;
-        run += rbuf[i];
-        if (run > tl_) { y = i; break; }
+      for (int i = c0; i < c1 && y < 0; i += VN) {
+        float r[VN];
+        if (i + VN <= c1) {
+          r_vec(i, r);
+        } else {
+#pragma unroll
+          for (int k = 0; k < VN; ++k) r[k] = (i + k < c1) ? r_at(i + k) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < VN; ++k) {
+          if (y < 0 && i + k < c1) {
+            if (r[k] > 0.f) last = i + k;
+            run += r[k];
+            if (run > tl_) y = i + k;
+          }
+        }
       }
       if (y < 0) y = last;  // rounding inside the chunk: its last nonzero entry
       if (y >= 0) { s_y = s0 + y; s_found = 1; }
@@ -372,7 +574,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs A) {
     if (!s_found) {  // t rounded past this slice's scan: the slice's last nonzero entry
       int last = -1;
       for (int i = c0; i < c1; ++i)
-        if (rbuf[i] > 0.f) last = i;
+        if (r_at(i) > 0.f) last = i;
       if (last >= 0) atomicMax(&s_last, last);
       __syncthreads();
       if (tid == 0) s_y = s0 + s_last;
@@ -391,39 +593,9 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const SampleArgs A) {
   if (A.residual != nullptr && valid) {
     const float inv = static_cast<float>(1.0 / R);
     float* out = A.residual + static_cast<long long>(b) * V;
-    for (int i = tid; i < len; i += kThreads) out[s0 + i] = rbuf[i] * inv;
+    for (int i = tid; i < len; i += kThreads) out[s0 + i] = r_at(i) * inv;
   }
   cluster.sync();  // #3: keep shared memory alive until every CTA has read slice_sum
-}
-
-template <typename K>
-int max_cluster(K kernel, int threads, size_t smem) {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return 8;
-  if (cached[dev] == 0) {
-    int best = 8;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-        cudaSuccess) {
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 16;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.gridDim = dim3(16);
-      cfg.blockDim = dim3(threads);
-      cfg.dynamicSmemBytes = smem;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n > 0) best = 16;
-    }
-    (void)cudaGetLastError();
-    cached[dev] = best;
-  }
-  return cached[dev];
 }
 
 template <typename T, bool kVec>
@@ -436,18 +608,25 @@ int launch(SampleArgs A, int B, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPECDEC_ERR_CUDA;
   if (!attr_set[dev]) {
     const cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSliceBytes);
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
     if (e != cudaSuccess) return map_cuda_error(e);
     attr_set[dev] = true;
   }
   constexpr int VN = Vec<T>::N;
-  // Smallest cluster whose slices fit shared memory, then split further while the grid is below
-  // two waves and slices stay >= 2048 elements.
-  int C = 1;
-  while (static_cast<long long>((V_ceil(A.V, C, VN))) * 4 > kMaxSliceBytes) C *= 2;
-  const int cap = max_cluster(kernel, kThreads, kMaxSliceBytes);
-  if (C > cap) return SPECDEC_ERR_UNSUPPORTED;
-  while (C * 2 <= cap && static_cast<long long>(B) * C < 2LL * sms && A.V / (2 * C) >= 2048) C *= 2;
+  // The largest cluster (up to 16 CTAs, slices >= 2048 elements, at most one CTA per SM) for
+  // which the B clusters are all resident at once, but at least the smallest one whose two
+  // staged rows fit the ring.
+  auto staged_bytes = [&](int c) {
+    return 2LL * ((static_cast<long long>(V_ceil(A.V, c, VN)) * sizeof(T) + 127) / 128 * 128);
+  };
+  int c_min = 1;
+  while (c_min <= 16 && staged_bytes(c_min) > kRingBytes) ++c_min;
+  if (c_min > 16) return SPECDEC_ERR_UNSUPPORTED;
+  static int active[64 * 17] = {0};
+  // One CTA per SM: at most sms / B CTAs per row.
+  const int c_max = max(c_min, std::min(std::min(16, A.V / 2048), sms / max(B, 1)));
+  const int C = cluster_for_one_wave(reinterpret_cast<const void*>(kernel), B, c_min, c_max,
+                                     kThreads, kRingBytes, active);
   A.C = C;
   A.slice = V_ceil(A.V, C, VN);
   cudaLaunchConfig_t cfg = {};
@@ -458,7 +637,7 @@ int launch(SampleArgs A, int B, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(B) * C);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(A.slice) * sizeof(float);
+  cfg.dynamicSmemBytes = kRingBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -483,12 +662,14 @@ extern "C" int specdec_verify_sample(const void* target_logits, const void* draf
   if (!target_logits || !draft_logits || !draft || !uniforms || !accept_len || !out_token ||
       !dev_status)
     return SPECDEC_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(target_logits) % es || reinterpret_cast<uintptr_t>(draft_logits) % es)
+  if (reinterpret_cast<uintptr_t>(target_logits) % es ||
+      reinterpret_cast<uintptr_t>(draft_logits) % es)
     return SPECDEC_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * (D + 1) * row_stride > (1LL << 47) || B > (1 << 26))
     return SPECDEC_ERR_UNSUPPORTED;
   const bool vec = reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&
-                   reinterpret_cast<uintptr_t>(draft_logits) % 16 == 0 && (row_stride * es) % 16 == 0;
+                   reinterpret_cast<uintptr_t>(draft_logits) % 16 == 0 &&
+                   (row_stride * es) % 16 == 0;
   SampleArgs A = {target_logits, draft_logits, D, V, row_stride, temperature, 1, V, draft,
                   uniforms, accept_len, out_token, residual_out, dev_status};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
