@@ -143,6 +143,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def captured_traffic(kernel: str, algorithmic_bytes: float):
+    """DRAM traffic per launch from the committed ncu capture of ``kernel``, scaled to this
+    launch's algorithmic bytes; None when the kernel source changed since the capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+                return None
+        ratio = (rec["dram_read_bytes"] + rec["dram_write_bytes"]) / rec["algorithmic_bytes"]
+        return round(ratio * algorithmic_bytes)
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -302,7 +318,8 @@ def run_specdec(args, rank, ws, local):
         "e2e": e2e,
         "roofline": {"bound": "hbm", "kernel": "realign", "achieved": round(achieved, 1),
                      "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": captured_traffic("realign_kernel", realign_bytes),
                      "bytes_per_launch": realign_bytes, "ms_per_launch": t_realign},
         "verify": {"ms_per_launch": t_verify, "bytes_per_launch": verify_bytes,
                    "achieved_gbs": round(verify_gbs, 1), "frac": round(verify_gbs / peak, 4)},
