@@ -173,7 +173,7 @@ def measured_peaks():
 def workload(args):
     import dataclasses
     from speculative_decoding_specdec_gb300 import synth
-    w = synth.WORKLOADS[args.workload]
+    w = synth.WORKLOADS["exspec_pool" if args.workload == "exspec_sweep" else args.workload]
     return dataclasses.replace(w, layers=args.layers) if args.layers else w
 
 
@@ -184,8 +184,6 @@ def run_specdec(args, rank, ws, local):
     from speculative_decoding_specdec_gb300.engine import EqspecBatch
 
     w = workload(args)
-    if w.mode == "pool":
-        raise SystemExit("the pool workload is benchmarked by its own script section (not yet)")
     dev = torch.device("cuda", torch.cuda.current_device())
     K, Wm = args.steps, args.warmup
     R = K + Wm
@@ -329,6 +327,141 @@ def run_specdec(args, rank, ws, local):
     }
 
 
+# ------------------------------------------------------------------------------ EXSPEC pool
+
+def run_pool(args, rank, ws):
+    """EXSPEC SequencePool rounds: grouping by length, one greedy verification over the pool,
+    then per batch an in-place commit (uniform batch) or gather + append (mixed leftovers).  The
+    verification pass that would write the new K/V columns between gather and append belongs to
+    the model and is not run; the copies move the same bytes either way."""
+    import numpy as np
+    import torch
+    from speculative_decoding_specdec_gb300 import synth
+    from speculative_decoding_specdec_gb300.engine import ExspecPool
+
+    w = workload(args)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    K, Wm = args.steps, args.warmup
+    R = K + Wm
+    gen = synth.make_gen(w.seed * 1000 + rank)
+    n0 = w.prompt_lengths(gen)
+    alpha = torch.rand(w.B, generator=gen) * 0.4 + 0.5          # per-sequence acceptance U[0.5, 0.9]
+    prompts = [torch.randint(0, w.V, (int(n),), generator=gen).tolist() for n in n0]
+    need = (int(n0.sum()) + w.B * (R * (w.D + 1) + w.D + 1)) * w.token_bytes
+    free, _ = torch.cuda.mem_get_info()
+    if need > 0.85 * free:
+        raise SystemExit(f"pool arena needs {need / 1e9:.0f} GB, {free / 1e9:.0f} GB free: "
+                         f"fewer rounds (--steps/--warmup)")
+    pool = ExspecPool(w.layers, w.heads, w.head_dim, w.kv_dtype, prompts, w.D, R, device=dev)
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    logits, drafts = [], []
+    for _ in range(R):
+        lg, d = synth.greedy_round(g, w.B, w.D, w.V, alpha.to(dev), dtype=w.logit_dtype, device=dev)
+        logits.append(lg)
+        drafts.append(d)
+    stream = torch.cuda.current_stream()
+    moved, uniform_frac, mixed_rows, kern = [], [], [], []
+
+    def one_round(r, timed):
+        n_before = pool.slot_len.cpu().numpy() if timed else None
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)] if timed else None
+        batches = pool.schedule()
+        if timed:
+            ev[0].record(stream)
+        pool.verify_greedy(logits[r], drafts[r])
+        for off, k, uni in batches:
+            pool.gather(off, k, uni)
+            pool.append(off, k, uni, drafts[r])
+        if timed:
+            ev[1].record(stream)
+            kern.append(ev)
+            perm = pool.perm.cpu().numpy()
+            n_after = pool.slot_len.cpu().numpy()
+            cols = 0
+            for off, k, uni in batches:
+                if not uni:
+                    rows = perm[off:off + k]
+                    cols += int((n_before[rows] - 1).sum() + (n_after[rows] - n_before[rows]).sum())
+            moved.append(2 * cols * w.token_bytes)
+            nu = sum(k for _, k, uni in batches if uni)
+            uniform_frac.append(nu / w.B)
+            mixed_rows.append(w.B - nu)
+
+    for r in range(Wm):
+        one_round(r, False)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for i in range(K):
+        one_round(Wm + i, True)
+    torch.cuda.synchronize()
+    wall = max_over_ranks(time.perf_counter() - t0, ws)
+    if int(pool.status.item()):
+        raise RuntimeError(f"device status {int(pool.status.item())}")
+    kern_ms = [e[0].elapsed_time(e[1]) for e in kern]
+    peak, peak_kind = measured_peaks()
+    gbs = sum(moved) / (sum(kern_ms) / 1e3) / 1e9
+    return {"value": sum_over_ranks(float(K), ws) / wall, "ms_per_step": wall / K * 1e3,
+            "kernel_ms_per_round": float(np.mean(kern_ms)),
+            "realign_gbs": round(gbs, 1), "realign_frac": round(gbs / peak, 4),
+            "peak": peak, "peak_source": peak_kind,
+            "uniform_row_fraction_per_round": [round(x, 3) for x in uniform_frac],
+            "mixed_rows_per_round": mixed_rows}
+
+
+# ------------------------------------------------------------------------------ batch sweep
+
+def run_sweep(args, rank, ws):
+    """EQSPEC rounds on the contiguous layout for B = 1..64 (Vicuna-7B-shaped cache, pool length
+    distribution): per B the realignment time, the bytes it moves (surviving columns only) and
+    the bytes a padded-row copy would move (2 * B * W' * P_tok), whose growth with B is the
+    superlinear term."""
+    import numpy as np
+    import torch
+    from speculative_decoding_specdec_gb300 import synth
+    from speculative_decoding_specdec_gb300.engine import EqspecBatch
+
+    base = synth.WORKLOADS["exspec_pool"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    K, Wm = args.steps, args.warmup
+    R = K + Wm
+    peak, peak_kind = measured_peaks()
+    out = []
+    for B in (1, 2, 4, 8, 16, 32, 64):
+        gen = synth.make_gen(base.seed * 100 + B)
+        n0 = synth.lengths_discrete(gen, B, base.prompt[1])
+        prompts = [torch.randint(0, base.V, (int(n),), generator=gen).tolist() for n in n0]
+        cap = int(n0.max()) + R * (base.D + 1) + base.D + 1
+        eng = EqspecBatch(base.layers, base.heads, base.head_dim, base.kv_dtype, B, base.D, cap, R,
+                          device=dev)
+        g = torch.Generator(device=dev).manual_seed(B)
+        rounds = [synth.greedy_round(g, B, base.D, base.V, 0.7, dtype=base.logit_dtype, device=dev)
+                  for _ in range(R)]
+        eng.start(prompts)
+        stream = torch.cuda.current_stream()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R)]
+        for r, (lg, d) in enumerate(rounds):
+            eng.verify_greedy(lg, d)
+            ev[r][0].record(stream)
+            eng.realign(d)
+            ev[r][1].record(stream)
+        torch.cuda.synchronize()
+        ms = [ev[r][0].elapsed_time(ev[r][1]) for r in range(Wm, R)]
+        nh = eng.n_hist.cpu().numpy().astype(np.int64)
+        wh = eng.w_hist.cpu().numpy().astype(np.int64)[:, 0]
+        alg = [2.0 * (nh[r + 1] - 1).sum() * base.token_bytes for r in range(Wm, R)]
+        padded = [2.0 * B * (wh[r + 1] - 1) * base.token_bytes for r in range(Wm, R)]
+        gbs = sum(alg) / (sum(ms) / 1e3) / 1e9
+        out.append({"B": B, "realign_ms_per_round": round(float(np.mean(ms)), 4),
+                    "realign_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                    "moved_gb_per_round": round(float(np.mean(alg)) / 1e9, 3),
+                    "padded_copy_gb_per_round": round(float(np.mean(padded)) / 1e9, 3),
+                    "mean_width": round(float(np.mean(wh[Wm + 1:R + 1])), 1)})
+        del eng, rounds
+        torch.cuda.empty_cache()
+    return {"sweep": out, "peak": peak, "peak_source": peak_kind}
+
+
 # ------------------------------------------------------------------------------ CPU oracle
 
 def oracle_round_sampler(wname, seed=0, layers_sample=2):
@@ -425,6 +558,27 @@ def main():
                         cpu_baseline=res["cpu_baseline"], dtype="f64",
                         e2e={"value": res["value"], "unit": "rounds/s",
                              "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0})
+            print(json.dumps(line))
+        return
+    if args.workload == "exspec_pool":
+        res = run_pool(args, rank, ws)
+        if rank == 0:
+            config["workload"] = (f"exspec_pool: {w.B} sequences, L={w.layers} KV heads={w.heads} "
+                                  f"head_dim={w.head_dim}, D={w.D}, V={w.V}, prompts from "
+                                  f"{{256,...,2048}}, acceptance U[0.5,0.9] per sequence, "
+                                  f"batches of 8, greedy verify")
+            line.update(value=res.pop("value"), ms_per_step=res.pop("ms_per_step"), pool=res,
+                        unit="pool rounds/s", metric="EXSPEC pool rounds/s")
+            print(json.dumps(line))
+        return
+    if args.workload == "exspec_sweep":
+        res = run_sweep(args, rank, ws)
+        if rank == 0:
+            config["workload"] = ("exspec_sweep: EQSPEC verify+realign on the contiguous layout, "
+                                  "Vicuna-7B-shaped cache, prompts from {256,...,2048}, D=5, "
+                                  "V=32000, B in 1..64")
+            line.update(metric="EQSPEC realign batch sweep", unit="ms/round", value=None,
+                        higher_is_better=False, **res)
             print(json.dumps(line))
         return
     res = run_specdec(args, rank, ws, local)

@@ -227,6 +227,8 @@ int specdec_group_by_length(const int32_t* lengths, int N, int batch_size, int m
  *   slot columns [N_s - 1, N_s + a_i) = scratch row i columns [W - 1, W + a_i) (not copied in
  *   place); pool_ids[s][N_s .. N_s + a_i) = d_1..d_{a_i}, pool_ids[s][N_s + a_i] = y_i;
  *   slot_len[s] = N_s + a_i + 1, with N_s = batch_len[i] as the gather recorded it.
+ *   by_slot != 0: accept_len, out_token and draft are pool-wide arrays indexed by slot s =
+ *   rows[i] (e.g. one verification call over the whole pool) instead of by batch row i.
  *   Errors: a_i outside [0, D], a recorded width/length out of range (INPUT_RANGE; nothing
  *   written).
  * Limits: 1 <= n_rows <= min(1024, scratch.rows), 1 <= D <= 31, arena.rows == 1, arena and
@@ -249,9 +251,10 @@ typedef struct {
   int32_t* scratch_ids;         /* [R][Sc] written by gather (may be NULL when in_place) */
   uint8_t* scratch_mask;        /* [R][Sc] */
   int32_t* scratch_pos;         /* [R][Sc] */
-  const int32_t* accept_len;    /* [n_rows] append only */
-  const int32_t* out_token;     /* [n_rows] append only */
-  const int32_t* draft;         /* [n_rows][D] append only */
+  const int32_t* accept_len;    /* [n_rows] (or [S] with by_slot) append only */
+  const int32_t* out_token;     /* [n_rows] (or [S] with by_slot) append only */
+  const int32_t* draft;         /* [n_rows][D] (or [S][D] with by_slot) append only */
+  int by_slot;                  /* append: index the three arrays above by slot */
   int32_t* dev_status;          /* [1] */
 } specdec_pool_args;
 

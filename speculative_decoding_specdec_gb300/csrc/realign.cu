@@ -53,7 +53,7 @@ struct ByteView {
 
 struct Params {
   ByteView src, dst;
-  int mode, R, D, L, H, col_bytes, tile, stages, copy_engine, in_place;
+  int mode, R, D, L, H, col_bytes, tile, stages, copy_engine, in_place, by_slot;
   int32_t pad_id;
   // EQSPEC
   const int32_t* n_committed;
@@ -175,8 +175,8 @@ __device__ bool build_plan(const Params& p, Plan& s, int* red) {
   } else {  // kPoolAppend
     const int W = *p.bwidth;
     for (int r = threadIdx.x; r < R; r += kThreads) {
-      const int N = p.batch_len[r], a = p.accept_len[r];
       const int sl = p.rows[r], c0 = p.slot_col[sl], cap = p.slot_cap[sl];
+      const int N = p.batch_len[r], a = p.accept_len[p.by_slot ? sl : r];
       if (a < 0 || a > D || N < 1 || N > W || c0 < 0 || cap > p.arena_cap - c0) bad |= 1;
       else if (N + a + 1 > p.ids_cap || N + a > cap) bad |= 2;
       s.aux[r] = N;
@@ -381,9 +381,10 @@ __device__ void write_metadata(const Params& p, const Plan& s, long long gt, lon
     for (int r = lt; r < p.R; r += ln) {
       const int sl = p.rows[r];
       const int N = s.aux[r], a = s.acc[r];
+      const int src = p.by_slot ? sl : r;  // row of accept_len / out_token / draft
       int32_t* ids = p.pool_ids + static_cast<long long>(sl) * p.ids_cap;
-      for (int q = 0; q < a; ++q) ids[N + q] = p.draft[static_cast<long long>(r) * p.D + q];
-      ids[N + a] = p.out_token[r];
+      for (int q = 0; q < a; ++q) ids[N + q] = p.draft[static_cast<long long>(src) * p.D + q];
+      ids[N + a] = p.out_token[src];
       p.slot_len[sl] = N + a + 1;
     }
   }
@@ -525,6 +526,7 @@ int pool_common(const specdec_pool_args* a, Params& p, bool append) {
   p.col_bytes = ar.head_dim * elem_size(ar.dtype);
   p.copy_engine = 0;
   p.in_place = a->in_place ? 1 : 0;
+  p.by_slot = a->by_slot ? 1 : 0;
   p.pad_id = a->pad_id;
   p.accept_len = a->accept_len;
   p.out_token = a->out_token;

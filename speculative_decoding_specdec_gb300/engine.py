@@ -93,3 +93,98 @@ class EqspecBatch:
                         pad_id=self.pad_id, copy_engine=copy_engine, stream=stream)
         self.cur = d
         self.round = r + 1
+
+
+class ExspecPool:
+    """Caller-side state of an EXSPEC SequencePool (one GPU).
+
+    Slots are unpadded at rest in one arena [L, 2, 1, H, sum(cap_s), hd]: slot s owns columns
+    [slot_col[s], slot_col[s] + cap_s) and holds the K/V of its first N_s - 1 tokens.  A round
+    groups the slots by length (uniform batches of ``batch_size`` equal-length rows first, then
+    mixed leftovers), verifies every slot's drafts in one call, and then per batch either commits
+    in place (uniform batch) or gathers the rows into the padded batch buffer and appends the
+    accepted columns back (mixed batch).  The schedule is read back to the host once per round:
+    it decides which calls follow.
+    """
+
+    def __init__(self, layers, heads, head_dim, kv_dtype, prompts, D, rounds, batch_size=8,
+                 device="cuda", pad_id=0):
+        dev = torch.device(device)
+        self.S = len(prompts)
+        self.D, self.bs, self.pad_id = D, batch_size, pad_id
+        n0 = [len(p) for p in prompts]
+        if min(n0) < 1:
+            raise ValueError("empty prompt")
+        grow = rounds * (D + 1) + D + 1
+        caps = [n + grow for n in n0]
+        cols = [0]
+        for c in caps[:-1]:
+            cols.append(cols[-1] + c)
+        self.max_len = max(caps)
+        self.arena = torch.empty((layers, 2, 1, heads, sum(caps), head_dim), dtype=kv_dtype,
+                                 device=dev)
+        sc_cap = max(n0) + grow
+        self.scratch = torch.empty((layers, 2, batch_size, heads, sc_cap, head_dim), dtype=kv_dtype,
+                                   device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.slot_col = torch.tensor(cols, **i32)
+        self.slot_cap = torch.tensor(caps, **i32)
+        self.slot_len = torch.tensor(n0, **i32)
+        self.pool_ids = torch.full((self.S, self.max_len), pad_id, **i32)
+        for s, p in enumerate(prompts):
+            self.pool_ids[s, :len(p)] = torch.as_tensor(p, dtype=torch.int32)
+        self.scratch_ids = torch.zeros((batch_size, sc_cap), **i32)
+        self.scratch_mask = torch.zeros((batch_size, sc_cap), dtype=torch.uint8, device=dev)
+        self.scratch_pos = torch.zeros((batch_size, sc_cap), **i32)
+        self.batch_len = torch.zeros(batch_size, **i32)
+        self.width = torch.zeros(1, **i32)
+        self.perm = torch.zeros(self.S, **i32)
+        self.offsets = torch.zeros(self.S + 1, **i32)
+        self.uniform = torch.zeros(self.S, dtype=torch.uint8, device=dev)
+        self.counts = torch.zeros(2, **i32)  # num_batches, num_uniform
+        self.accept_len = torch.zeros(self.S, **i32)
+        self.out_token = torch.zeros(self.S, **i32)
+        self.status = torch.zeros(1, **i32)
+        self._host = torch.zeros(2 + (self.S + 1) + self.S, dtype=torch.int32).pin_memory()
+
+    def schedule(self, stream=None):
+        """Group the slots by length on the device; returns the batches as (offset, rows, uniform)
+        after one small device-to-host copy."""
+        specdec.group_by_length(self.slot_len, self.bs, self.max_len, self.perm, self.offsets,
+                                self.uniform, self.counts[0:1], self.counts[1:2], self.status,
+                                stream)
+        h = self._host
+        S = self.S
+        h[0:2].copy_(self.counts, non_blocking=True)
+        h[2:3 + S].copy_(self.offsets, non_blocking=True)
+        h[3 + S:].copy_(self.uniform.to(torch.int32), non_blocking=True)
+        (stream or torch.cuda.current_stream()).synchronize()
+        nb = int(h[0])
+        off = h[2:3 + S].tolist()
+        uni = h[3 + S:].tolist()
+        return [(off[k], off[k + 1] - off[k], bool(uni[k])) for k in range(nb)]
+
+    def verify_greedy(self, logits, draft, stream=None):
+        """Greedy verification of every slot: logits [S, D+1, V], draft [S, D] in slot order."""
+        specdec.verify_greedy(logits, draft, self.accept_len, self.out_token, self.status, stream)
+
+    def verify_sample(self, target_logits, draft_logits, draft, uniforms, temperature,
+                      stream=None):
+        specdec.verify_sample(target_logits, draft_logits, draft, uniforms, temperature,
+                              self.accept_len, self.out_token, self.status, None, stream)
+
+    def gather(self, off, n, uniform, stream=None):
+        """Repad batch perm[off:off+n] into the batch buffer (uniform batches: lengths only)."""
+        rows = self.perm[off:off + n]
+        specdec.pool_gather(self.arena, self.scratch, rows, self.D, self.slot_col, self.slot_cap,
+                            self.slot_len, self.pool_ids, self.batch_len[:n], self.width,
+                            self.status, self.scratch_ids, self.scratch_mask, self.scratch_pos,
+                            pad_id=self.pad_id, in_place=uniform, stream=stream)
+
+    def append(self, off, n, uniform, draft, stream=None):
+        """Commit batch perm[off:off+n] back to its slots (pool-wide accept lengths and tokens)."""
+        rows = self.perm[off:off + n]
+        specdec.pool_append(self.arena, self.scratch, rows, self.D, self.slot_col, self.slot_cap,
+                            self.slot_len, self.pool_ids, self.batch_len[:n], self.width,
+                            self.accept_len, self.out_token, draft, self.status,
+                            in_place=uniform, by_slot=True, stream=stream)

@@ -54,7 +54,7 @@ class PoolArgs(ctypes.Structure):
                 ("scratch_ids", ctypes.c_void_p), ("scratch_mask", ctypes.c_void_p),
                 ("scratch_pos", ctypes.c_void_p), ("accept_len", ctypes.c_void_p),
                 ("out_token", ctypes.c_void_p), ("draft", ctypes.c_void_p),
-                ("dev_status", ctypes.c_void_p)]
+                ("by_slot", ctypes.c_int), ("dev_status", ctypes.c_void_p)]
 
 
 _vp, _ll, _i, _f = ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_float
@@ -258,10 +258,12 @@ def pool_gather(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids,
 
 
 def pool_append(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len, width,
-                accept_len, out_token, draft, status, in_place=False, stream=None):
-    """Append a verified batch back to its pool slots (see specdec.h)."""
+                accept_len, out_token, draft, status, in_place=False, by_slot=False, stream=None):
+    """Append a verified batch back to its pool slots (see specdec.h).  With ``by_slot`` the
+    accept lengths, tokens and drafts are pool-wide arrays indexed by slot."""
     a = _pool_args(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len,
                    width, status, 0, in_place)
+    a.by_slot = int(bool(by_slot))
     for name, t in (("accept_len", accept_len), ("out_token", out_token), ("draft", draft)):
         _need(t, torch.int32, name)
         setattr(a, name, t.data_ptr())

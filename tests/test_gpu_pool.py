@@ -160,3 +160,63 @@ def test_capacity_and_range_errors():
                    st)
     torch.cuda.synchronize()
     assert int(st.item()) == 5 and torch.equal(before, P["slot_len"])
+
+
+def test_pool_engine_rounds_match_oracle():
+    """ExspecPool rounds (grouping, one verification over the pool, per-batch gather/append with
+    pool-wide accept lengths) against the oracle, with a synthetic verification pass writing the
+    new K/V columns in between; every slot equals its from-scratch rebuild after every round."""
+    from speculative_decoding_specdec_gb300.engine import ExspecPool
+    gen = synth.make_gen(24)
+    L, H, hd, D, V, S, bs, rounds = 1, 2, 16, 3, 40, 22, 4, 4
+    n0 = synth.lengths_discrete(gen, S, [4, 6, 9]).tolist()
+    toks = [torch.randint(0, V, (n,), generator=gen).tolist() for n in n0]
+    pool = ExspecPool(L, H, hd, torch.float32, toks, D, rounds, batch_size=bs)
+    pool.arena.fill_(-9.0)
+    cols = pool.slot_col.cpu().numpy()
+    for s in range(S):
+        synth.write_tagged_columns(pool.arena, 0, int(cols[s]), s, list(range(n0[s] - 1)),
+                                   toks[s][:-1])
+    n = np.array(n0)
+    saw_uniform = saw_mixed = False
+    for _ in range(rounds):
+        batches = pool.schedule()
+        ep, eo, eu, enu = O.group_by_length(n, bs)
+        assert [(int(eo[k]), int(eo[k + 1] - eo[k]), bool(eu[k])) for k in range(len(eu))] == batches
+        np.testing.assert_array_equal(pool.perm.cpu().numpy(), ep)
+        logits, draft = synth.greedy_round(gen, S, D, V, 0.6, dtype=torch.float32)
+        dd = draft.cuda()
+        pool.verify_greedy(logits.cuda(), dd)
+        a, y = O.verify_greedy(logits.double().numpy(), draft.numpy())
+        for off, k, uniform in batches:
+            rows = ep[off:off + k].tolist()
+            pool.gather(off, k, uniform)
+            torch.cuda.synchronize()
+            W = int(pool.width.item())
+            assert W == max(n[s] for s in rows)
+            for i, s in enumerate(rows):       # the verification pass writes [pending, d_1..d_D]
+                pos = list(range(n[s] - 1, n[s] + D))
+                tk = [toks[s][-1]] + draft[s].tolist()
+                if uniform:
+                    synth.write_tagged_columns(pool.arena, 0, int(cols[s]) + n[s] - 1, s, pos, tk)
+                else:
+                    synth.write_tagged_columns(pool.scratch, i, W - 1, s, pos, tk)
+            pool.append(off, k, uniform, dd)
+            torch.cuda.synchronize()
+            assert int(pool.status.item()) == 0
+            for s in rows:
+                toks[s] = toks[s] + draft[s, :a[s]].tolist() + [int(y[s])]
+                n[s] += a[s] + 1
+            saw_uniform |= uniform
+            saw_mixed |= not uniform
+        np.testing.assert_array_equal(pool.slot_len.cpu().numpy(), n)
+        np.testing.assert_array_equal(pool.accept_len.cpu().numpy(), a)
+        arena = pool.arena[:, :, 0].cpu().numpy()
+        ids = pool.pool_ids.cpu().numpy()
+        for s in range(S):
+            ref = torch.zeros(L, 2, 1, H, n[s] - 1, hd)
+            synth.write_tagged_columns(ref, 0, 0, s, list(range(n[s] - 1)), toks[s][:-1])
+            c0 = int(cols[s])
+            np.testing.assert_array_equal(arena[:, :, :, c0:c0 + n[s] - 1], ref[:, :, 0].numpy())
+            assert list(ids[s, :n[s]]) == toks[s]
+    assert saw_uniform and saw_mixed
