@@ -21,7 +21,12 @@
  *
  * Conventions for every entry point:
  *   - All array arguments are DEVICE pointers owned by the caller.  The library allocates no
- *     memory and keeps no state between calls; calls on different streams are independent.
+ *     memory and keeps no state between calls.  Greedy verification also takes a caller-owned
+ *     device WORKSPACE (size from specdec_verify_greedy_workspace, 256-byte aligned) through which
+ *     its CTAs exchange per-row results.  Zero-fill it once before its first use: every call
+ *     leaves it all zero again (also when it reports an out-of-range input through dev_status),
+ *     so it is reused as is, for any shape it is large enough for.  Calls that may overlap on the
+ *     GPU need separate workspaces (one per stream).
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the legacy
  *     default stream).  The return value reports host-detected problems only: an invalid
  *     argument, an unsupported configuration, or a failed launch.  It does not wait for the GPU.
@@ -36,6 +41,7 @@
 #ifndef SPECDEC_H
 #define SPECDEC_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -79,14 +85,24 @@ const char* specdec_status_string(int status);
  *   accept_len [B] int32 out: a_b = number of leading drafts equal to the target's choice.
  *   out_token  [B] int32 out: y_b = the target's choice at row a_b (the replacement when a_b < D,
  *              the bonus token when a_b == D).  The cycle commits a_b + 1 tokens.
+ *   workspace  device buffer of at least specdec_verify_greedy_workspace(B, D) bytes, all zero
+ *              (see the conventions above).
  * The target's choice of a row is its maximum score, lowest token index on ties; NaN scores are
  * never chosen (a row of only NaN sets SPECDEC_ERR_INPUT_RANGE).  A draft id outside [0, V) sets
  * SPECDEC_ERR_INPUT_RANGE and counts as a mismatch.
- * Limits: B >= 0, 1 <= D <= 31, 1 <= V, row_stride >= V.
+ * Limits: B >= 0, 1 <= D <= 31, 1 <= V, row_stride >= V; a NULL, unaligned or too small
+ * workspace is SPECDEC_ERR_INVALID_ARG; more than 2^40 bytes of scores is
+ * SPECDEC_ERR_UNSUPPORTED.
  */
 int specdec_verify_greedy(const void* logits, int dtype, int B, int D, int V,
                           long long row_stride, const int32_t* draft, int32_t* accept_len,
-                          int32_t* out_token, int32_t* dev_status, void* stream);
+                          int32_t* out_token, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream);
+
+/* Workspace bytes specdec_verify_greedy needs for B rows of D drafts (0 for an invalid shape):
+ * one 64-bit key per score row and one 32-bit counter per batch row, each array 256-byte
+ * aligned. */
+size_t specdec_verify_greedy_workspace(int B, int D);
 
 /*
  * Sampled verification (speculative rejection sampling).  [IE5, "Exactness Means Different

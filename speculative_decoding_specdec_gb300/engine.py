@@ -13,6 +13,26 @@ import torch
 from . import specdec
 
 
+class Workspaces:
+    """Zero-filled verification workspaces, one per kind, grown on demand (a workspace is left
+    zero-filled by every call, so one buffer serves every shape it is large enough for)."""
+
+    def __init__(self, device):
+        self.device = device
+        self._ws = {}
+
+    def get(self, kind, nbytes):
+        ws = self._ws.get(kind)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            self._ws[kind] = ws
+        return ws
+
+    def greedy(self, logits, draft):
+        B, D = draft.shape
+        return self.get("greedy", specdec.greedy_workspace_bytes(B, D))
+
+
 class EqspecBatch:
     def __init__(self, layers, heads, head_dim, kv_dtype, B, D, cap, max_rounds, device="cuda",
                  pad_id=0):
@@ -30,6 +50,7 @@ class EqspecBatch:
         self.accept_len = torch.zeros(B, dtype=torch.int32, device=dev)
         self.out_token = torch.zeros(B, dtype=torch.int32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.workspaces = Workspaces(dev)
         self.round = 0
         self.cur = 0
 
@@ -75,7 +96,8 @@ class EqspecBatch:
 
     # ------------------------------------------------------------------ one round
     def verify_greedy(self, logits, draft, stream=None):
-        specdec.verify_greedy(logits, draft, self.accept_len, self.out_token, self.status, stream)
+        specdec.verify_greedy(logits, draft, self.accept_len, self.out_token, self.status,
+                              self.workspaces.greedy(logits, draft), stream)
 
     def verify_sample(self, target_logits, draft_logits, draft, uniforms, temperature,
                       residual=None, stream=None):
@@ -145,6 +167,7 @@ class ExspecPool:
         self.accept_len = torch.zeros(self.S, **i32)
         self.out_token = torch.zeros(self.S, **i32)
         self.status = torch.zeros(1, **i32)
+        self.workspaces = Workspaces(dev)
         self._host = torch.zeros(2 + (self.S + 1) + self.S, dtype=torch.int32).pin_memory()
 
     def schedule(self, stream=None):
@@ -166,7 +189,8 @@ class ExspecPool:
 
     def verify_greedy(self, logits, draft, stream=None):
         """Greedy verification of every slot: logits [S, D+1, V], draft [S, D] in slot order."""
-        specdec.verify_greedy(logits, draft, self.accept_len, self.out_token, self.status, stream)
+        specdec.verify_greedy(logits, draft, self.accept_len, self.out_token, self.status,
+                              self.workspaces.greedy(logits, draft), stream)
 
     def verify_sample(self, target_logits, draft_logits, draft, uniforms, temperature,
                       stream=None):

@@ -62,8 +62,11 @@ lib.specdec_version.restype = _i
 lib.specdec_version.argtypes = []
 lib.specdec_status_string.restype = ctypes.c_char_p
 lib.specdec_status_string.argtypes = [_i]
+_sz = ctypes.c_size_t
 lib.specdec_verify_greedy.restype = _i
-lib.specdec_verify_greedy.argtypes = [_vp, _i, _i, _i, _i, _ll, _vp, _vp, _vp, _vp, _vp]
+lib.specdec_verify_greedy.argtypes = [_vp, _i, _i, _i, _i, _ll, _vp, _vp, _vp, _vp, _sz, _vp, _vp]
+lib.specdec_verify_greedy_workspace.restype = _sz
+lib.specdec_verify_greedy_workspace.argtypes = [_i, _i]
 lib.specdec_realign.restype = _i
 lib.specdec_realign.argtypes = [ctypes.POINTER(RealignArgs), _vp]
 lib.specdec_group_by_length.restype = _i
@@ -142,18 +145,35 @@ def _score_rows(x, B, rows, name):
     return x.stride(1)
 
 
-def verify_greedy(logits, draft, accept_len, out_token, status, stream=None):
+def greedy_workspace_bytes(B, D) -> int:
+    """Workspace bytes greedy verification needs for B rows of D drafts."""
+    return int(lib.specdec_verify_greedy_workspace(int(B), int(D)))
+
+
+def _workspace(ws, need, name):
+    if ws is None or ws.dtype != torch.uint8 or not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError(f"{name}: workspace must be a contiguous CUDA uint8 tensor")
+    if ws.numel() < need:
+        raise ValueError(f"{name}: workspace of {ws.numel()} bytes, {need} needed")
+    return ctypes.c_void_p(ws.data_ptr()), ws.numel()
+
+
+def verify_greedy(logits, draft, accept_len, out_token, status, workspace, stream=None):
     """Greedy verification: logits [B, D+1, V] (fp32/bf16), draft [B, D] int32 ->
-    accept_len[B], out_token[B] int32 (written asynchronously on ``stream``)."""
+    accept_len[B], out_token[B] int32 (written asynchronously on ``stream``).  ``workspace``: a
+    zero-filled uint8 CUDA tensor of at least greedy_workspace_bytes(B, D) bytes; every call leaves
+    it zero-filled again, so it is reused as is."""
     B, D = draft.shape
     V = logits.shape[-1]
     rs = _score_rows(logits, B, D + 1, "logits")
     for t, n in ((draft, "draft"), (accept_len, "accept_len"), (out_token, "out_token"),
                  (status, "status")):
         _need(t, torch.int32, n)
+    wp, wn = _workspace(workspace, greedy_workspace_bytes(B, D) if B else 0,
+                        "verify_greedy")
     _check(lib.specdec_verify_greedy(_ptr(logits), dtype_code(logits.dtype), B, D, V, rs,
-                                     _ptr(draft), _ptr(accept_len), _ptr(out_token), _ptr(status),
-                                     _stream(stream)), "specdec_verify_greedy")
+                                     _ptr(draft), _ptr(accept_len), _ptr(out_token), wp, wn,
+                                     _ptr(status), _stream(stream)), "specdec_verify_greedy")
 
 
 def verify_sample(target_logits, draft_logits, draft, uniforms, temperature, accept_len,

@@ -70,12 +70,15 @@ def test_host_validation_codes():
     import speculative_decoding_specdec_gb300.specdec as sd
     L = sd.lib
     # verify_greedy: empty batch is a no-op; bad sizes and NULL pointers are caught on the host
-    assert L.specdec_verify_greedy(None, sd.BF16, 0, 4, 100, 100, None, None, None, None, None) == sd.OK
-    assert L.specdec_verify_greedy(None, sd.BF16, 1, 4, 100, 100, None, None, None, None, None) == sd.ERR_INVALID_ARG
-    assert L.specdec_verify_greedy(None, sd.BF16, 1, 0, 100, 100, None, None, None, None, None) == sd.ERR_INVALID_ARG
-    assert L.specdec_verify_greedy(None, sd.BF16, 1, 32, 100, 100, None, None, None, None, None) == sd.ERR_UNSUPPORTED
-    assert L.specdec_verify_greedy(None, 7, 1, 4, 100, 100, None, None, None, None, None) == sd.ERR_INVALID_ARG
-    assert L.specdec_verify_greedy(None, sd.F32, 1, 4, 100, 99, None, None, None, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_verify_greedy(None, sd.BF16, 0, 4, 100, 100, None, None, None, None, 0, None, None) == sd.OK
+    assert L.specdec_verify_greedy(None, sd.BF16, 1, 4, 100, 100, None, None, None, None, 0, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_verify_greedy(None, sd.BF16, 1, 0, 100, 100, None, None, None, None, 0, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_verify_greedy(None, sd.BF16, 1, 32, 100, 100, None, None, None, None, 0, None, None) == sd.ERR_UNSUPPORTED
+    assert L.specdec_verify_greedy(None, 7, 1, 4, 100, 100, None, None, None, None, 0, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_verify_greedy(None, sd.F32, 1, 4, 100, 99, None, None, None, None, 0, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_verify_greedy_workspace(0, 4) == 0                        # invalid shape
+    assert L.specdec_verify_greedy_workspace(3, 32) == 0
+    assert L.specdec_verify_greedy_workspace(3, 4) == 256 + 256               # keys, counters
     # realign: NULL args, empty batch, bad views
     assert L.specdec_realign(None, None) == sd.ERR_INVALID_ARG
     a = sd.RealignArgs()

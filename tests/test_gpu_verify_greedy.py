@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def gpu_greedy(logits, draft, row_stride=None):
+def gpu_greedy(logits, draft, row_stride=None, ws=None):
     import speculative_decoding_specdec_gb300.specdec as sd
     B, Dp1, V = logits.shape
     if row_stride is None:
@@ -27,7 +27,10 @@ def gpu_greedy(logits, draft, row_stride=None):
     a = torch.full((B,), -5, dtype=torch.int32, device=DEV)
     y = torch.full((B,), -5, dtype=torch.int32, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    sd.verify_greedy(x, draft.to(DEV), a, y, st)
+    if ws is None:
+        ws = torch.zeros(sd.greedy_workspace_bytes(B, Dp1 - 1), dtype=torch.uint8,
+                         device=DEV)
+    sd.verify_greedy(x, draft.to(DEV), a, y, st, ws)
     torch.cuda.synchronize()
     return a.cpu().numpy(), y.cpu().numpy(), int(st.item())
 
@@ -58,6 +61,8 @@ def check(logits, draft, row_stride=None):
     (1, 31, 4099, torch.float32, 0.9),         # D = 31
     (1, 1, 50000, torch.bfloat16, 0.5),        # B = 1, D = 1
     (33, 6, 151552, torch.bfloat16, 0.7),      # GLM-4-shaped vocabulary
+    (300, 3, 100, torch.bfloat16, 0.6),        # many batch rows per CTA share
+    (97, 2, 1003, torch.float32, 0.6),         # shares cross rows and batch rows, ragged V
 ])
 def test_greedy_matches_oracle(B, D, V, dtype, alpha):
     gen = synth.make_gen(1000 + B * 7 + D)
@@ -129,17 +134,52 @@ def test_out_of_range_draft_sets_status_and_mismatches():
 
 def test_empty_batch_and_host_errors():
     import speculative_decoding_specdec_gb300.specdec as sd
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device=DEV)
     x = torch.zeros(0, 5, 100, dtype=torch.bfloat16, device=DEV)
     d = torch.zeros(0, 4, dtype=torch.int32, device=DEV)
     z = torch.zeros(0, dtype=torch.int32, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    sd.verify_greedy(x, d, z, z, st)
+    sd.verify_greedy(x, d, z, z, st, ws)
     x = torch.zeros(1, 33, 100, dtype=torch.bfloat16, device=DEV)
     d = torch.zeros(1, 32, dtype=torch.int32, device=DEV)
     o = torch.zeros(1, dtype=torch.int32, device=DEV)
     with pytest.raises(sd.SpecdecError) as e:
-        sd.verify_greedy(x, d, o, o, st)
+        sd.verify_greedy(x, d, o, o, st, ws)
     assert e.value.code == sd.ERR_UNSUPPORTED
+    x = torch.zeros(8, 6, 32000, dtype=torch.bfloat16, device=DEV)   # workspace too small
+    d = torch.zeros(8, 5, dtype=torch.int32, device=DEV)
+    o = torch.zeros(8, dtype=torch.int32, device=DEV)
+    rc = sd.lib.specdec_verify_greedy(x.data_ptr(), sd.BF16, 8, 5, 32000, 32000, d.data_ptr(),
+                                      o.data_ptr(), o.data_ptr(), ws.data_ptr(), 64, st.data_ptr(),
+                                      None)
+    assert rc == sd.ERR_INVALID_ARG
+    rc = sd.lib.specdec_verify_greedy(x.data_ptr(), sd.BF16, 8, 5, 32000, 32000, d.data_ptr(),
+                                      o.data_ptr(), o.data_ptr(), ws.data_ptr() + 128, 1 << 19,
+                                      st.data_ptr(), None)
+    assert rc == sd.ERR_INVALID_ARG                                   # workspace not 256-aligned
+
+
+def test_workspace_reused_across_calls():
+    """One workspace, zero-filled once, serves consecutive calls of several shapes: every call
+    (including one that reports an out-of-range draft) leaves it all zero again."""
+    import speculative_decoding_specdec_gb300.specdec as sd
+    gen = synth.make_gen(9)
+    shapes = [(16, 4, 151936), (8, 5, 32000), (256, 5, 32000), (3, 3, 1003), (97, 2, 1003)]
+    need = max(sd.greedy_workspace_bytes(B, D) for B, D, V in shapes)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    for _ in range(2):
+        for B, D, V in shapes:
+            logits, draft = synth.greedy_round(gen, B, D, V, 0.6, dtype=torch.bfloat16)
+            a, y, st = gpu_greedy(logits, draft, ws=ws)
+            ea, ey = oracle_greedy(logits, draft)
+            assert st == 0
+            np.testing.assert_array_equal(a, ea)
+            np.testing.assert_array_equal(y, ey)
+            assert int(ws.count_nonzero()) == 0
+    logits, draft = synth.greedy_round(gen, 4, 4, 3000, 1.0, dtype=torch.bfloat16)
+    draft[1, 2] = 3000
+    _, _, st = gpu_greedy(logits, draft, ws=ws)
+    assert st == 5 and int(ws.count_nonzero()) == 0
 
 
 def test_repeated_calls_deterministic():
