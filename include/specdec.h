@@ -50,6 +50,7 @@ extern "C" {
 
 #define SPECDEC_VERSION 100  /* 1.0.0 */
 #define SPECDEC_MAX_DRAFT 31 /* D <= 31: D+1 rows fit one warp ballot */
+#define SPECDEC_GREEDY_SCRATCH_BYTES 73728 /* static scratch of specdec_verify_greedy_noalloc */
 
 typedef enum {
   SPECDEC_OK = 0,
@@ -103,6 +104,29 @@ int specdec_verify_greedy(const void* logits, int dtype, int B, int D, int V,
  * one 64-bit key per score row and one 32-bit counter per batch row, each array 256-byte
  * aligned. */
 size_t specdec_verify_greedy_workspace(int B, int D);
+
+/*
+ * Greedy verification without a caller workspace.  The pages have no counterpart: this is an
+ * interface convenience, not part of the method.  It computes exactly what specdec_verify_greedy
+ * computes (same arguments minus the workspace, same results, limits and status codes) for
+ * callers that cannot allocate device memory or keep a buffer alive between calls: a host that
+ * links this C library alone and has no device allocator of its own, or a plugin that a serving
+ * framework hands raw device pointers while keeping every allocation to itself.
+ *
+ * Scratch: one static device array of SPECDEC_GREEDY_SCRATCH_BYTES per device, inside this
+ * library.  It is zero when the library is loaded, and every call leaves it zero again, which is
+ * the state the next call needs.  The first call on a device looks up the array's address
+ * (cudaGetSymbolAddress, with that device current on the calling thread) and keeps it; make that
+ * first call before any stream capture.  Later calls use the device current on the calling thread.
+ * A shape whose workspace, specdec_verify_greedy_workspace(B, D), exceeds
+ * SPECDEC_GREEDY_SCRATCH_BYTES is SPECDEC_ERR_UNSUPPORTED (for example B = 1024 with D = 7 fits; B = 4096
+ * with D = 5 does not).  Calls that may overlap on one device (other streams, other
+ * host threads) share the array and race: run them on one stream, or use specdec_verify_greedy
+ * with one workspace per stream.  Returns SPECDEC_ERR_CUDA if the address lookup fails.
+ */
+int specdec_verify_greedy_noalloc(const void* logits, int dtype, int B, int D, int V,
+                                  long long row_stride, const int32_t* draft, int32_t* accept_len,
+                                  int32_t* out_token, int32_t* dev_status, void* stream);
 
 /*
  * Sampled verification (speculative rejection sampling).  [IE5, "Exactness Means Different

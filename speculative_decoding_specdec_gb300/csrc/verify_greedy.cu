@@ -21,6 +21,7 @@
 // __ballot_sync/__ffs, writes a_b and y_b, and sets the keys and the ticket back to zero.  One
 // launch, no waiting between CTAs; the work is B*(D+1)*V*sizeof(score) bytes of HBM, read once.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -348,4 +349,51 @@ extern "C" int specdec_verify_greedy(const void* logits, int dtype, int B, int D
                                    dev_status, workspace, s)
              : launch<float, false>(logits, B, D, V, row_stride, draft, accept_len, out_token,
                                     dev_status, workspace, s);
+}
+
+// ------------------------------------------------------------------ variant without a workspace
+// The same launch on a static per-device scratch array instead of a caller workspace.  Static
+// device memory is zero when the module loads, and every greedy call leaves its workspace zero.
+namespace specdec {
+namespace {
+
+constexpr int kMaxDevices = 64;
+static __device__ __align__(256) unsigned char g_greedy_scratch[SPECDEC_GREEDY_SCRATCH_BYTES];
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices];  // the array's address on each device, looked up once
+
+int greedy_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return map_cuda_error(e);
+  if (dev < 0 || dev >= kMaxDevices) return SPECDEC_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_greedy_scratch);  // with device `dev` current
+    if (e != cudaSuccess) return map_cuda_error(e);
+    if (p == nullptr) return SPECDEC_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return SPECDEC_OK;
+}
+
+}  // namespace
+}  // namespace specdec
+
+extern "C" int specdec_verify_greedy_noalloc(const void* logits, int dtype, int B, int D, int V,
+                                             long long row_stride, const int32_t* draft,
+                                             int32_t* accept_len, int32_t* out_token,
+                                             int32_t* dev_status, void* stream) {
+  // Nothing to run, or sizes the workspace entry point rejects before it looks at a workspace.
+  if (B <= 0 || D < 1 || D > SPECDEC_MAX_DRAFT)
+    return specdec_verify_greedy(logits, dtype, B, D, V, row_stride, draft, accept_len, out_token,
+                                 nullptr, 0, dev_status, stream);
+  if (specdec::workspace_bytes(B, D) > SPECDEC_GREEDY_SCRATCH_BYTES) return SPECDEC_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  const int rc = specdec::greedy_scratch(&scratch);
+  if (rc != SPECDEC_OK) return rc;
+  return specdec_verify_greedy(logits, dtype, B, D, V, row_stride, draft, accept_len, out_token,
+                               scratch, SPECDEC_GREEDY_SCRATCH_BYTES, dev_status, stream);
 }

@@ -21,6 +21,7 @@ lib = ctypes.CDLL(LIB_PATH)
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_CAPACITY, ERR_INPUT_RANGE, ERR_TIMEOUT = range(7)
 F32, BF16 = 0, 1
 MAX_DRAFT = 31
+GREEDY_SCRATCH_BYTES = 73728   # SPECDEC_GREEDY_SCRATCH_BYTES
 
 c_i32p = ctypes.POINTER(ctypes.c_int32)
 
@@ -67,6 +68,8 @@ lib.specdec_verify_greedy.restype = _i
 lib.specdec_verify_greedy.argtypes = [_vp, _i, _i, _i, _i, _ll, _vp, _vp, _vp, _vp, _sz, _vp, _vp]
 lib.specdec_verify_greedy_workspace.restype = _sz
 lib.specdec_verify_greedy_workspace.argtypes = [_i, _i]
+lib.specdec_verify_greedy_noalloc.restype = _i
+lib.specdec_verify_greedy_noalloc.argtypes = [_vp, _i, _i, _i, _i, _ll, _vp, _vp, _vp, _vp, _vp]
 lib.specdec_realign.restype = _i
 lib.specdec_realign.argtypes = [ctypes.POINTER(RealignArgs), _vp]
 lib.specdec_group_by_length.restype = _i
@@ -174,6 +177,22 @@ def verify_greedy(logits, draft, accept_len, out_token, status, workspace, strea
     _check(lib.specdec_verify_greedy(_ptr(logits), dtype_code(logits.dtype), B, D, V, rs,
                                      _ptr(draft), _ptr(accept_len), _ptr(out_token), wp, wn,
                                      _ptr(status), _stream(stream)), "specdec_verify_greedy")
+
+
+def verify_greedy_noalloc(logits, draft, accept_len, out_token, status, stream=None):
+    """Greedy verification on the library's static per-device scratch instead of a workspace
+    (for callers that cannot allocate or keep a device buffer).  Calls that may overlap on one
+    device share that scratch: keep them on one stream."""
+    B, D = draft.shape
+    V = logits.shape[-1]
+    rs = _score_rows(logits, B, D + 1, "logits")
+    for t, n in ((draft, "draft"), (accept_len, "accept_len"), (out_token, "out_token"),
+                 (status, "status")):
+        _need(t, torch.int32, n)
+    _check(lib.specdec_verify_greedy_noalloc(_ptr(logits), dtype_code(logits.dtype), B, D, V, rs,
+                                             _ptr(draft), _ptr(accept_len), _ptr(out_token),
+                                             _ptr(status), _stream(stream)),
+           "specdec_verify_greedy_noalloc")
 
 
 def verify_sample(target_logits, draft_logits, draft, uniforms, temperature, accept_len,

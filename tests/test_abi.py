@@ -13,16 +13,25 @@ HEADER = os.path.join(ROOT, "include", "specdec.h")
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|const char\s*\*)\s+(specdec_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\s*\*)\s+(specdec_\w+)\s*\(", text, re.M)))
 
 
 def test_every_declared_symbol_is_exported():
     import speculative_decoding_specdec_gb300.specdec as sd
     names = declared_functions()
     assert "specdec_realign" in names and "specdec_verify_sample" in names
+    assert "specdec_verify_greedy_workspace" in names and "specdec_verify_greedy_noalloc" in names
     missing = [n for n in names if not hasattr(sd.lib, n)]
     assert missing == []
     assert sd.version() == 100
+
+
+def test_header_constants_match_binding():
+    import speculative_decoding_specdec_gb300.specdec as sd
+    text = open(HEADER).read()
+    macro = {m: int(v) for m, v in re.findall(r"^#define (SPECDEC_\w+) (\d+)", text, re.M)}
+    assert macro["SPECDEC_MAX_DRAFT"] == sd.MAX_DRAFT
+    assert macro["SPECDEC_GREEDY_SCRATCH_BYTES"] == sd.GREEDY_SCRATCH_BYTES
 
 
 def test_status_strings():
@@ -77,6 +86,11 @@ def test_host_validation_codes():
     assert L.specdec_verify_greedy(None, 7, 1, 4, 100, 100, None, None, None, None, 0, None, None) == sd.ERR_INVALID_ARG
     assert L.specdec_verify_greedy(None, sd.F32, 1, 4, 100, 99, None, None, None, None, 0, None, None) == sd.ERR_INVALID_ARG
     assert L.specdec_verify_greedy_workspace(0, 4) == 0                        # invalid shape
+    # the workspace-free variant applies the same host checks before it touches a device
+    assert L.specdec_verify_greedy_noalloc(None, sd.BF16, 0, 4, 100, 100, None, None, None, None, None) == sd.OK
+    assert L.specdec_verify_greedy_noalloc(None, sd.BF16, 1, 0, 100, 100, None, None, None, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_verify_greedy_noalloc(None, sd.BF16, 1, 32, 100, 100, None, None, None, None, None) == sd.ERR_UNSUPPORTED
+    assert L.specdec_verify_greedy_noalloc(None, sd.BF16, 4096, 5, 100, 100, None, None, None, None, None) == sd.ERR_UNSUPPORTED
     assert L.specdec_verify_greedy_workspace(3, 32) == 0
     assert L.specdec_verify_greedy_workspace(3, 4) == 256 + 256               # keys, counters
     # realign: NULL args, empty batch, bad views
