@@ -40,6 +40,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--layers", type=int, default=0,
                    help="override the workload's layer count (smaller cache, e.g. for ncu)")
+    p.add_argument("--no-cpu-baseline", action="store_true",
+                   help="skip timing the oracle (cpu_baseline: null), e.g. under a profiler")
     return p.parse_args()
 
 
@@ -584,7 +586,7 @@ def main():
     res = run_specdec(args, rank, ws, local)
     if rank == 0:
         cpu = None
-        if ws == 1:
+        if ws == 1 and not args.no_cpu_baseline:
             rps, rounds, Ls, _ = time_oracle(args.workload, budget_s=12.0)
             cpu = {"value": rps, "unit": "rounds/s", "cores": 1, "kind": "oracle",
                    "sample": f"{rounds} rounds: verification of all rows, realignment of {Ls} of "
