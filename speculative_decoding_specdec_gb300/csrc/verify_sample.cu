@@ -69,9 +69,34 @@ __device__ __forceinline__ float pow2f(float k) {
   if (!(k >= -126.f)) return 0.f;
   return __int_as_float((static_cast<int>(k) + 127) << 23);
 }
-__device__ __forceinline__ double pow2d(float k) {
-  if (!(k >= -1022.f)) return 0.0;
-  return __longlong_as_double(static_cast<long long>(static_cast<int>(k) + 1023) << 52);
+
+// Float-float values hi + lo (|lo| <= ulp(hi)/2) summed with Knuth's TwoSum: the cross-block
+// totals keep about 44 bits with fp32 instructions only (fp64 throughput is low on this GPU).
+// The addition is commutative, so an xor-butterfly leaves the same bits in every lane.
+struct ff {
+  float hi, lo;
+};
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  const float s = a.hi + b.hi;
+  const float v = s - a.hi;
+  const float e = ((a.hi - (s - v)) + (b.hi - v)) + (a.lo + b.lo);
+  const float h = s + e;
+  return ff{h, e - (h - s)};
+}
+__device__ __forceinline__ double ff_to_double(float2 a) {
+  return static_cast<double>(a.x) + static_cast<double>(a.y);
+}
+// Merge per-lane (offset o, sum S) pairs of a warp: the largest offset M and the sum scaled to
+// it (power-of-two scalings are exact).
+__device__ __forceinline__ void warp_merge_ff(float o, ff S, float& M, ff& T) {
+  M = o;
+#pragma unroll
+  for (int k = 16; k > 0; k >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, k));
+  const float sc = pow2f(o - M);
+  T = ff{S.hi * sc, S.lo * sc};
+#pragma unroll
+  for (int k = 16; k > 0; k >>= 1)
+    T = ff_add(T, ff{__shfl_xor_sync(0xffffffffu, T.hi, k), __shfl_xor_sync(0xffffffffu, T.lo, k)});
 }
 
 // Merge (oo, os) into (o, s): both sums are relative to their integer offsets.
@@ -183,13 +208,15 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A)
   __shared__ float po[kMaxQ][kWarps];
   __shared__ float ps[kMaxQ][kWarps];
   __shared__ float co[kMaxQ];   // this CTA's per-row partials, read by the whole cluster
-  __shared__ double cs[kMaxQ];
+  __shared__ float2 cs[kMaxQ];  // (hi, lo)
   __shared__ float go[kMaxQ];   // cluster-combined per-row offset and normaliser
-  __shared__ double gs[kMaxQ];
+  __shared__ float2 gs[kMaxQ];
   __shared__ float incl[kThreads];
   __shared__ float wtot[32];
-  __shared__ double slice_sum[2];  // this CTA's residual total (second slot: fallback to p)
+  __shared__ float slice_sum[2];  // this CTA's residual total (second slot: fallback to p)
   __shared__ double s_R, s_P;
+  __shared__ float s_tl, s_inv, s_iz, s_iw;
+  __shared__ int s_owner, s_valid;
   __shared__ int s_a, s_bad, s_found, s_y, s_last, s_fail;
   __shared__ __align__(8) uint64_t full[kMaxRingStages], empty[kMaxRingStages], pbar;
   __shared__ StreamPlan plan;
@@ -339,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A)
   }
   __syncthreads();
   if (s_fail && tid == 0) set_status(A.status, SPECDEC_ERR_TIMEOUT);
-  for (int q = warp; q < Q; q += kAllWarps) {  // CTA partial per row (fp64), plus the tail
+  for (int q = warp; q < Q; q += kAllWarps) {  // CTA partial per row, plus the tail
     float o = lane < kWarps ? po[q][lane] : kOffsetNone;
     float s = lane < kWarps ? ps[q][lane] : 0.f;
     if (lane == kWarps && kVec) {  // elements past the streamed body (fewer than one vector)
@@ -349,13 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A)
         fold<1>(&x, c2, o, s);
       }
     }
-    float M = o;
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, k));
-    double S = static_cast<double>(s) * pow2d(o - M);
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1) S += __shfl_xor_sync(0xffffffffu, S, k);
-    if (lane == 0) { co[q] = M; cs[q] = S; }
+    float M;
+    ff S;
+    warp_merge_ff(o, ff{s, 0.f}, M, S);
+    if (lane == 0) { co[q] = M; cs[q] = make_float2(S.hi, S.lo); }
   }
   cluster.sync();  // #1: every CTA's partials are final
 
@@ -364,23 +388,20 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A)
   // partial through distributed shared memory (C <= 16), then a warp reduction.
   for (int q = warp; q < Q; q += kAllWarps) {
     const float o = lane < C ? cluster.map_shared_rank(co, lane)[q] : kOffsetNone;
-    const double sp = lane < C ? cluster.map_shared_rank(cs, lane)[q] : 0.0;
-    float M = o;
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, k));
-    double S = sp * pow2d(o - M);
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1) S += __shfl_xor_sync(0xffffffffu, S, k);
+    const float2 sp = lane < C ? cluster.map_shared_rank(cs, lane)[q] : make_float2(0.f, 0.f);
+    float M;
+    ff S;
+    warp_merge_ff(o, ff{sp.x, sp.y}, M, S);
     if (lane == 0) {
       go[q] = M;
-      gs[q] = S;
+      gs[q] = make_float2(S.hi, S.lo);
     }
   }
   __syncthreads();
   if (warp == 0) {
     bool bad = false;
-    for (int q = lane; q < Q; q += 32)
-      if (!(gs[q] > 0.0) || !isfinite(gs[q])) bad = true;  // NaN/+inf scores or an empty row
+    for (int q = lane; q < Q; q += 32)  // NaN/+inf scores or an empty row
+      if (!(gs[q].x > 0.f) || !isfinite(gs[q].x) || !isfinite(gs[q].y)) bad = true;
     bool accept = true;
     if (lane < D) {
       const int d = pre_d[lane];
@@ -395,12 +416,30 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A)
         if (w == kNegInf) {
           accept = true;  // q(d) = 0
         } else {
-          // p(d)/q(d) = 2^(z*c2 - o_p) / S_p  /  (2^(w*c2 - o_q) / S_q), in fp64
-          const double c2d = static_cast<double>(c2);
-          const double e = (static_cast<double>(z) - static_cast<double>(w)) * c2d -
-                           (static_cast<double>(go[lane]) - static_cast<double>(go[D + 1 + lane]));
-          const double ratio = exp2(e) * (gs[D + 1 + lane] / gs[lane]);
-          accept = static_cast<double>(u) < ratio;
+          // p(d)/q(d) = 2^e * S_q / S_p with e = (z - w)*c2 - (o_p - o_q).  Estimate it in fp32:
+          // e as an exact float-float (TwoProd by fmaf, TwoSum), 2^e by ex2.approx of its
+          // fraction (relative error below 1e-6 in all).  Decide from the estimate when it is
+          // clear by a margin of 4e-6 (relative), otherwise in fp64.
+          const float op = go[lane], oq = go[D + 1 + lane];
+          const float dz = z - w;
+          const float ph = dz * c2, pl = fmaf(dz, c2, -ph);
+          const ff e = ff_add(ff{ph, pl}, ff{oq - op, 0.f});
+          const float n = rintf(e.hi);
+          const float f = (e.hi - n) + e.lo;
+          const float r = ldexpf(ex2(f), static_cast<int>(n)) * (gs[D + 1 + lane].x / gs[lane].x);
+          const bool exact_in = fabsf(op) < 4.0e6f && fabsf(oq) < 4.0e6f && isfinite(dz);
+          if (exact_in && r > 1.00001f) {
+            accept = true;  // ratio above 1: every u in [0, 1) accepts
+          } else if (exact_in && r < 1e-30f && u > 1e-29f) {
+            accept = false;  // ratio below 1e-30 and u above twice its bound
+          } else if (exact_in && r >= 1e-30f && fabsf(u - r) > 4e-6f * r) {
+            accept = u < r;
+          } else {
+            const double ed = (static_cast<double>(z) - static_cast<double>(w)) * static_cast<double>(c2) -
+                              (static_cast<double>(op) - static_cast<double>(oq));
+            accept = static_cast<double>(u) <
+                     exp2(ed) * (ff_to_double(gs[D + 1 + lane]) / ff_to_double(gs[lane]));
+          }
         }
       }
     }
@@ -411,8 +450,11 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A)
     const unsigned rej = __ballot_sync(0xffffffffu, lane < D && !accept);
     const bool any_bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
-      s_a = rej ? __ffs(static_cast<int>(rej)) - 1 : D;
+      const int a = rej ? __ffs(static_cast<int>(rej)) - 1 : D;
+      s_a = a;
       s_bad = any_bad ? 1 : 0;
+      s_iz = 1.f / (gs[a].x + gs[a].y);
+      s_iw = a < D ? 1.f / (gs[D + 1 + a].x + gs[D + 1 + a].y) : 0.f;
     }
   }
   __syncthreads();
@@ -447,9 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A)
   __syncthreads();
   if (s_fail && tid == 0) set_status(A.status, SPECDEC_ERR_TIMEOUT);
   const float oz = go[a];
-  const float iz = static_cast<float>(1.0 / gs[a]);
+  const float iz = s_iz;
   const float ow = resid ? go[D + 1 + a] : 0.f;
-  const float iw = resid ? static_cast<float>(1.0 / gs[D + 1 + a]) : 0.f;
+  const float iw = s_iw;
   bool use_p = !resid;
   auto r_at = [&](int i) -> float {
     const float p = ex2(fmaf(Vec<T>::scalar(zs + i), c2, -oz)) * iz;
@@ -514,19 +556,19 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A)
     return incl[kThreads - 1];
   };
   auto exchange = [&](int slot, float Rc) {  // R over the cluster and this CTA's offset
-    if (tid == 0) slice_sum[slot] = static_cast<double>(Rc);
+    if (tid == 0) slice_sum[slot] = Rc;
     cluster.sync();
     if (warp == 0) {
-      const double x = lane < C ? cluster.map_shared_rank(slice_sum, lane)[slot] : 0.0;
-      double R = 0.0, P = 0.0;  // rank order in every CTA: P_c + Rc_c == P_{c+1} bit for bit
+      const float x = lane < C ? cluster.map_shared_rank(slice_sum, lane)[slot] : 0.f;
+      ff R{0.f, 0.f}, P{0.f, 0.f};  // rank order in every CTA: P_c + Rc_c == P_{c+1} bit for bit
       for (int r = 0; r < C; ++r) {
-        const double xr = __shfl_sync(0xffffffffu, x, r);
-        if (r < rank) P += xr;
-        R += xr;
+        const float xr = __shfl_sync(0xffffffffu, x, r);
+        if (r == rank) P = R;
+        R = ff_add(R, ff{xr, 0.f});
       }
       if (lane == 0) {
-        s_R = R;
-        s_P = P;
+        s_R = ff_to_double(make_float2(R.hi, R.lo));
+        s_P = ff_to_double(make_float2(P.hi, P.lo));
       }
     }
     __syncthreads();
@@ -539,13 +581,19 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A)
     Rc = scan();
     exchange(1, Rc);  // #2b
   }
-  const double R = s_R, P = s_P;
-  const float u_draw = pre_u[D];
-  const double t = static_cast<double>(u_draw) * R;
-  const bool valid = (R > 0.0) && isfinite(R) && !s_bad;
-  const bool owner = valid && Rc > 0.f && P <= t && t < P + static_cast<double>(Rc);
-  if (owner) {
-    const float tl_ = static_cast<float>(t - P);
+  if (tid == 0) {  // the draw's scalar arithmetic in fp64, on one thread
+    const double R = s_R, P = s_P;
+    const double t = static_cast<double>(pre_u[D]) * R;
+    const bool ok = (R > 0.0) && isfinite(R) && !s_bad;
+    s_valid = ok ? 1 : 0;
+    s_owner = (ok && Rc > 0.f && P <= t && t < P + static_cast<double>(Rc)) ? 1 : 0;
+    s_tl = static_cast<float>(t - P);
+    s_inv = ok ? static_cast<float>(1.0 / R) : 0.f;
+  }
+  __syncthreads();
+  const bool valid = s_valid != 0;
+  if (s_owner) {
+    const float tl_ = s_tl;
     const float E = tid ? incl[tid - 1] : 0.f;
     if (E <= tl_ && tl_ < incl[tid]) {
       float run = E;
@@ -591,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A)
     A.out_token[b] = -1;
   }
   if (A.residual != nullptr && valid) {
-    const float inv = static_cast<float>(1.0 / R);
+    const float inv = s_inv;
     float* out = A.residual + static_cast<long long>(b) * V;
     for (int i = tid; i < len; i += kThreads) out[s0 + i] = r_at(i) * inv;
   }
