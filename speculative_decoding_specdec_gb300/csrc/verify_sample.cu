@@ -8,8 +8,10 @@
 //   the cycle, and a fully accepted draft earns a bonus token from the distribution after it.
 //
 // GB300 mapping.  One thread-block cluster of C CTAs per batch row b (C <= 16, chosen so the grid
-// fills one wave of resident CTAs); CTA c owns the vocabulary
-// slice [c*slice, (c+1)*slice).
+// fills one wave of resident CTAs); CTA c owns the vocabulary slice [c*slice, (c+1)*slice).  A
+// CTA is either 16 consumer warps with a 192 KB ring (one per SM) or 8 with a 96 KB ring (two per
+// SM), whichever lets the B clusters keep more SMs busy (clusters stay inside one GPC, so the
+// usable cluster sizes differ between the two).
 //  Phase 1  a producer thread streams the slice of the 2D+1 score rows (D+1 target, D draft)
 //           through a 192 KB shared-memory ring in 32 KB cp.async.bulk copies (rows stored back
 //           to back are read as one contiguous range per CTA; its idle lanes meanwhile fetch
@@ -39,11 +41,17 @@ namespace cg = cooperative_groups;
 namespace specdec {
 namespace {
 
-constexpr int kWarps = 16;                    // consumer warps
-constexpr int kAllWarps = kWarps + 1;         // plus the producer warp
-constexpr int kThreads = kAllWarps * 32;
-constexpr int kConsumers = kWarps * 32;
-constexpr int kRingBytes = 192 * 1024;  // one CTA per SM, six 32 KB stages
+// Two shapes of CTA: W = 16 consumer warps with a 192 KB ring (one CTA per SM) or W = 8 with a
+// 96 KB ring (two per SM).  The launch takes the one whose clusters keep more SMs busy.
+template <int W>
+struct Cfg {
+  static constexpr int kWarps = W;                // consumer warps
+  static constexpr int kAllWarps = W + 1;         // plus the producer warp
+  static constexpr int kThreads = kAllWarps * 32;
+  static constexpr int kConsumers = W * 32;
+  static constexpr int kRingBytes = W * 12288;    // W/16 * 192 KB: 32 KB stages
+  static constexpr int kPerSm = 16 / W;           // CTAs per SM
+};
 constexpr int kChunkBytes = 32768;      // bytes per bulk copy
 constexpr int kMaxQ = 2 * SPECDEC_MAX_DRAFT + 1;  // score rows per batch row
 constexpr float kLog2e = 1.4426950408889634f;     // log2(e)
@@ -202,8 +210,11 @@ struct SampleArgs {
   int32_t* status;
 };
 
-template <typename T, bool kVec>
-__global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A) {
+template <typename T, bool kVec, int W>
+__global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kernel(const SampleArgs A) {
+  constexpr int kWarps = Cfg<W>::kWarps, kAllWarps = Cfg<W>::kAllWarps;
+  constexpr int kThreads = Cfg<W>::kThreads, kConsumers = Cfg<W>::kConsumers;
+  constexpr int kRingBytes = Cfg<W>::kRingBytes;
   extern __shared__ __align__(128) char dyn[];  // phase 1: the ring; phase 3: two staged rows
   __shared__ float po[kMaxQ][kWarps];
   __shared__ float ps[kMaxQ][kWarps];
@@ -646,35 +657,52 @@ __global__ void __launch_bounds__(kThreads, 1) sample_kernel(const SampleArgs A)
   cluster.sync();  // #3: keep shared memory alive until every CTA has read slice_sum
 }
 
-template <typename T, bool kVec>
-int launch(SampleArgs A, int B, cudaStream_t stream) {
-  auto kernel = sample_kernel<T, kVec>;
+// The cluster size configuration W would use for this shape, and how many SMs it keeps busy.
+struct Choice {
+  int C = 0;
+  double sms_busy = -1.0;
+};
+
+template <typename T, bool kVec, int W>
+int prepare(const SampleArgs& A, int B, Choice* ch) {
+  auto kernel = sample_kernel<T, kVec, W>;
   const int sms = sm_count();
   if (sms <= 0) return SPECDEC_ERR_CUDA;
   static bool attr_set[64] = {false};
+  static int active[64 * 17] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPECDEC_ERR_CUDA;
   if (!attr_set[dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+    const cudaError_t e = cudaFuncSetAttribute(
+        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<W>::kRingBytes);
     if (e != cudaSuccess) return map_cuda_error(e);
     attr_set[dev] = true;
   }
   constexpr int VN = Vec<T>::N;
-  // The largest cluster (up to 16 CTAs, slices >= 2048 elements, at most one CTA per SM) for
+  // The largest cluster (up to 16 CTAs, slices >= 2048 elements, at most kPerSm CTAs per SM) for
   // which the B clusters are all resident at once, but at least the smallest one whose two
   // staged rows fit the ring.
   auto staged_bytes = [&](int c) {
     return 2LL * ((static_cast<long long>(V_ceil(A.V, c, VN)) * sizeof(T) + 127) / 128 * 128);
   };
   int c_min = 1;
-  while (c_min <= 16 && staged_bytes(c_min) > kRingBytes) ++c_min;
-  if (c_min > 16) return SPECDEC_ERR_UNSUPPORTED;
-  static int active[64 * 17] = {0};
-  // One CTA per SM: at most sms / B CTAs per row.
-  const int c_max = max(c_min, std::min(std::min(16, A.V / 2048), sms / max(B, 1)));
+  while (c_min <= 16 && staged_bytes(c_min) > Cfg<W>::kRingBytes) ++c_min;
+  if (c_min > 16) return SPECDEC_OK;  // not possible with this configuration
+  const int slots = sms * Cfg<W>::kPerSm;
+  const int c_max = max(c_min, std::min(std::min(16, A.V / 2048), slots / max(B, 1)));
   const int C = cluster_for_one_wave(reinterpret_cast<const void*>(kernel), B, c_min, c_max,
-                                     kThreads, kRingBytes, active);
+                                     Cfg<W>::kThreads, Cfg<W>::kRingBytes, active);
+  const long long ctas = static_cast<long long>(B) * C;
+  const long long waves = (ctas + slots - 1) / slots;
+  ch->C = C;
+  ch->sms_busy = static_cast<double>(ctas) / Cfg<W>::kPerSm / static_cast<double>(waves);
+  return SPECDEC_OK;
+}
+
+template <typename T, bool kVec, int W>
+int launch(SampleArgs A, int B, int C, cudaStream_t stream) {
+  auto kernel = sample_kernel<T, kVec, W>;
+  constexpr int VN = Vec<T>::N;
   A.C = C;
   A.slice = V_ceil(A.V, C, VN);
   cudaLaunchConfig_t cfg = {};
@@ -684,12 +712,25 @@ int launch(SampleArgs A, int B, cudaStream_t stream) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(B) * C);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kRingBytes;
+  cfg.blockDim = dim3(Cfg<W>::kThreads);
+  cfg.dynamicSmemBytes = Cfg<W>::kRingBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return map_cuda_error(cudaLaunchKernelEx(&cfg, kernel, A));
+}
+
+template <typename T, bool kVec>
+int launch(SampleArgs A, int B, cudaStream_t stream) {
+  Choice one, two;  // W = 16 (one CTA per SM) and W = 8 (two per SM)
+  int rc = prepare<T, kVec, 16>(A, B, &one);
+  if (rc != SPECDEC_OK) return rc;
+  rc = prepare<T, kVec, 8>(A, B, &two);
+  if (rc != SPECDEC_OK) return rc;
+  if (one.C == 0 && two.C == 0) return SPECDEC_ERR_UNSUPPORTED;
+  if (two.C != 0 && two.sms_busy > one.sms_busy * 1.05)
+    return launch<T, kVec, 8>(A, B, two.C, stream);
+  return launch<T, kVec, 16>(A, B, one.C, stream);
 }
 
 }  // namespace

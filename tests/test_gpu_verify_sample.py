@@ -79,6 +79,7 @@ def compare(tl, dl, draft, u, T, row_stride=None, max_excused=0.02):
     (2, 31, 600, 0.9, torch.float32),         # D = 31
     (1, 2, 9, 0.7, torch.float32),            # tiny V
     (64, 2, 4096, 0.7, torch.bfloat16),       # many rows
+    (16, 4, 151936, 0.7, torch.bfloat16),     # Qwen3-8B-shaped: two CTAs per SM, clusters of 13
 ])
 def test_sample_matches_oracle(B, D, V, T, dtype):
     gen = synth.make_gen(2000 + B + D)
@@ -150,3 +151,11 @@ def test_host_errors():
         gpu_sample(tl, dl, draft, u, 0.0)
     with pytest.raises(sd.SpecdecError):
         gpu_sample(tl, dl, draft, u, float("inf"))
+
+
+def test_repeated_calls_deterministic():
+    gen = synth.make_gen(38)
+    tl, dl, draft, u = synth.sampled_round(gen, 32, 6, 151552, 0.7)
+    r1 = gpu_sample(tl, dl, draft, u, 0.7, residual=False)
+    r2 = gpu_sample(tl, dl, draft, u, 0.7, residual=False)
+    assert (r1[0] == r2[0]).all() and (r1[1] == r2[1]).all()
