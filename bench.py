@@ -321,8 +321,11 @@ def run_specdec(args, rank, ws, local):
                      "frac": round(achieved / peak, 4),
                      "traffic": captured_traffic("realign_kernel", realign_bytes),
                      "bytes_per_launch": realign_bytes, "ms_per_launch": t_realign},
-        "verify": {"ms_per_launch": t_verify, "bytes_per_launch": verify_bytes,
-                   "achieved_gbs": round(verify_gbs, 1), "frac": round(verify_gbs / peak, 4)},
+        "verify": {"kernel": "greedy_kernel" if w.mode == "greedy" else "sample_kernel",
+                   "ms_per_launch": t_verify, "bytes_per_launch": verify_bytes,
+                   "achieved_gbs": round(verify_gbs, 1), "frac": round(verify_gbs / peak, 4),
+                   "traffic": captured_traffic("greedy_kernel" if w.mode == "greedy"
+                                               else "sample_kernel", verify_bytes)},
         "committed_slots_per_s": committed / (ms_max / K / 1e3),
         "committed_per_round": committed,
         "cap_cols": cap,
