@@ -8,8 +8,10 @@
 //   rejected draft), and a fully accepted draft earns a bonus token from the last row.
 //
 // GB300 mapping.  The B*(D+1) score rows form one virtual sequence of 16-byte units (each row
-// padded to whole units); a grid of up to two CTAs per SM splits it into equal contiguous shares,
-// so every SM streams the same number of bytes whatever B, D and V are.  Inside a share each
+// padded to whole units); the grid splits it into equal contiguous shares, so every SM streams
+// the same number of bytes whatever B, D and V are.  Rows stored back to back are streamed by one
+// CTA per SM through a shared-memory ring of bulk copies (greedy_ring_kernel: the whole share is
+// in flight at once); other layouts by up to two CTAs per SM with 16-byte loads, where each
 // thread walks its units (one every kThreads) with a cursor that only adds, keeps 8 loads in
 // flight across row boundaries, and folds elements into a running best.  A best is a 64-bit key
 // (order-preserving score bits above the complemented index), so "higher score, then lower index"
@@ -24,6 +26,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "stream.cuh"
 
 namespace specdec {
 namespace {
@@ -133,6 +136,56 @@ struct Cursor {
   }
 };
 
+// After a CTA's row segments are final in s_key: merge them into the per-row keys of the
+// workspace, take one ticket per batch row touched, and decide the batch rows whose last ticket
+// this CTA took.  NT = threads of the CTA.
+template <int NT>
+__device__ void merge_and_decide(const GreedyArgs& A, const unsigned long long* s_key,
+                                 unsigned char* s_last, long long g0, long long g1, int nseg) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int Q = A.D + 1;
+  // Merge this CTA's row segments into the per-row keys, then take one ticket per batch row.
+  for (int s = tid; s < nseg; s += NT) {
+    if (s_key[s] != 0ull) red_max_gpu(&A.key[g0 + s], s_key[s]);
+    fence_acq_rel_gpu();
+  }
+  __syncthreads();
+  const long long b0 = g0 / Q, b1 = g1 / Q;
+  const int nb = static_cast<int>(b1 - b0 + 1);
+  for (int k = tid; k < nb; k += NT) {
+    const long long b = b0 + k;
+    const long long r0 = b * Q * A.RU, r1 = (b + 1) * Q * A.RU - 1;  // its units
+    const unsigned expected =
+        static_cast<unsigned>(A.split.owner(r1) - A.split.owner(r0) + 1);
+    s_last[k] = atom_add_acq_rel_gpu(&A.ticket[b], 1u) == expected - 1u ? 1 : 0;
+  }
+  __syncthreads();
+  for (int k = warp; k < nb; k += NT / 32) {
+    if (!s_last[k]) continue;
+    const long long b = b0 + k;
+    int g = -1;  // lane j: the target's choice of row j of batch row b
+    if (lane < Q) {
+      const unsigned long long key = ld_relaxed_gpu(&A.key[b * Q + lane]);
+      if (key != 0ull) g = static_cast<int>(~static_cast<uint32_t>(key));
+    }
+    const int D = A.D;
+    const int d = lane < D ? A.draft[b * D + lane] : 0;
+    const bool bad_draft = lane < D && (d < 0 || d >= A.V);
+    const bool mismatch = lane < D && (bad_draft || g != d);
+    const unsigned mm = __ballot_sync(0xffffffffu, mismatch);
+    const int a = mm ? __ffs(static_cast<int>(mm)) - 1 : D;
+    const int y = __shfl_sync(0xffffffffu, g, a);
+    const bool bad = bad_draft || (lane < Q && g < 0);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(A.status, SPECDEC_ERR_INPUT_RANGE);
+    if (lane < Q) A.key[b * Q + lane] = 0ull;  // ready for the next call
+    if (lane == 0) {
+      A.accept_len[b] = a;
+      A.out_token[b] = y;
+      A.ticket[b] = 0u;
+    }
+  }
+}
+
 template <typename T, bool kVec>
 __global__ void __launch_bounds__(kThreads, 2) greedy_kernel(const GreedyArgs A) {
   __shared__ unsigned long long s_key[kMaxSegs];
@@ -140,8 +193,7 @@ __global__ void __launch_bounds__(kThreads, 2) greedy_kernel(const GreedyArgs A)
 
   constexpr int VN = kVec ? Vec<T>::N : 1;
   const int c = blockIdx.x;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int Q = A.D + 1;
+  const int tid = threadIdx.x;
   const long long u0 = A.split.start(c), u1 = A.split.start(c + 1);
   const long long g0 = u0 / A.RU, g1 = (u1 - 1) / A.RU;  // first and last global row touched
   const int nseg = static_cast<int>(g1 - g0 + 1);
@@ -215,46 +267,114 @@ __global__ void __launch_bounds__(kThreads, 2) greedy_kernel(const GreedyArgs A)
   flush(prow);
   __syncthreads();
 
-  // Merge this CTA's row segments into the per-row keys, then take one ticket per batch row.
-  for (int s = tid; s < nseg; s += kThreads) {
-    if (s_key[s] != 0ull) red_max_gpu(&A.key[g0 + s], s_key[s]);
-    fence_acq_rel_gpu();
+  merge_and_decide<kThreads>(A, s_key, s_last, g0, g1, nseg);
+}
+
+
+// Rows stored back to back (row_stride == V, V a multiple of the vector width, 16-byte aligned):
+// one CTA per SM streams its share through a 192 KB shared-memory ring with cp.async.bulk copies
+// of up to 32 KB (cut at row ends) issued by one thread, so a whole share of up to ~190 KB is in
+// flight at once; 16 consumer warps fold the landed chunks.  Same keys, tickets and workspace.
+constexpr int kRingWarps = 16;
+constexpr int kRingThreads = (kRingWarps + 1) * 32;
+constexpr int kRingConsumers = kRingWarps * 32;
+constexpr int kRingChunk = 32768;
+constexpr int kRingStages = 6;
+constexpr int kRingBytes = kRingStages * kRingChunk;
+constexpr int kRingChunkUnits = kRingChunk / 16;
+
+template <typename T>
+__global__ void __launch_bounds__(kRingThreads, 1) greedy_ring_kernel(const GreedyArgs A) {
+  extern __shared__ __align__(128) char ring[];
+  __shared__ unsigned long long s_key[kMaxSegs];
+  __shared__ unsigned char s_last[kMaxSegs];
+  __shared__ __align__(8) uint64_t full[kRingStages], empty[kRingStages];
+  __shared__ int s_fail;
+
+  constexpr int VN = Vec<T>::N;
+  const int c = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int RU = A.RU;
+  const long long u0 = A.split.start(c), u1 = A.split.start(c + 1);
+  const long long g0 = u0 / RU, g1 = (u1 - 1) / RU;  // first and last global row touched
+  const int nseg = static_cast<int>(g1 - g0 + 1);
+  if (nseg > kMaxSegs) {  // excluded by the launch geometry
+    if (tid == 0) set_status(A.status, SPECDEC_ERR_UNSUPPORTED);
+    return;
+  }
+  for (int s = tid; s < nseg; s += kRingThreads) s_key[s] = 0ull;
+  if (tid == 0) {
+    s_fail = 0;
+    for (int k = 0; k < kRingStages; ++k) {
+      mbar_init(&full[k], 1);
+      mbar_init(&empty[k], kRingWarps);
+    }
+    fence_mbar_init();
   }
   __syncthreads();
-  const long long b0 = g0 / Q, b1 = g1 / Q;
-  const int nb = static_cast<int>(b1 - b0 + 1);
-  for (int k = tid; k < nb; k += kThreads) {
-    const long long b = b0 + k;
-    const long long r0 = b * Q * A.RU, r1 = (b + 1) * Q * A.RU - 1;  // its units
-    const unsigned expected =
-        static_cast<unsigned>(A.split.owner(r1) - A.split.owner(r0) + 1);
-    s_last[k] = atom_add_acq_rel_gpu(&A.ticket[b], 1u) == expected - 1u ? 1 : 0;
+  const char* base = static_cast<const char*>(A.logits);  // unit u at base + 16 u
+  // Segment k: units [lo, hi) of row g0 + k.
+  auto seg_lo = [&](int k) { return static_cast<int>(max(u0, (g0 + k) * RU) - (g0 + k) * RU); };
+  auto seg_hi = [&](int k) { return static_cast<int>(min(u1, (g0 + k + 1) * RU) - (g0 + k) * RU); };
+
+  if (warp == kRingWarps) {
+    if (lane == 0) {  // producer: every segment's chunks, in order, through the ring
+      int n = 0;
+      bool ok = true;
+      for (int k = 0; k < nseg && ok; ++k) {
+        const int lo = seg_lo(k), hi = seg_hi(k);
+        const char* src = base + ((g0 + k) * RU + lo) * 16;
+        for (int off = 0; off < hi - lo; off += kRingChunkUnits, ++n) {
+          const int st = n % kRingStages, r = n / kRingStages;
+          if (r > 0 && !mbar_wait_sleep(&empty[st], static_cast<uint32_t>((r - 1) & 1), kSleepTries,
+                                        kSleepNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bytes = static_cast<uint32_t>(min(kRingChunkUnits, hi - lo - off)) * 16u;
+          mbar_arrive_expect_tx(&full[st], bytes);
+          bulk_g2s(ring + st * kRingChunk, src + static_cast<long long>(off) * 16, bytes, &full[st]);
+        }
+      }
+      if (!ok) s_fail = 1;
+      for (int m = max(0, n - kRingStages); m < n; ++m)  // no copy outlives the kernel
+        (void)mbar_wait_sleep(&full[m % kRingStages], static_cast<uint32_t>((m / kRingStages) & 1),
+                              kSleepTries, kSleepNs);
+    }
+  } else {
+    int n = 0;
+    bool ok = true;
+    for (int k = 0; k < nseg && ok; ++k) {
+      const int lo = seg_lo(k), hi = seg_hi(k);
+      float bv = 0.f;
+      int bi = -1;
+      for (int off = 0; off < hi - lo; off += kRingChunkUnits, ++n) {
+        const int st = n % kRingStages, r = n / kRingStages;
+        const bool got =
+            mbar_wait_sleep(&full[st], static_cast<uint32_t>(r & 1), kSleepTries, kSleepNs);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const int cu = min(kRingChunkUnits, hi - lo - off);
+        const uint4* v4 = reinterpret_cast<const uint4*>(ring + st * kRingChunk);
+        const int e0 = (lo + off) * VN;  // vocabulary index of the chunk's first element
+#pragma unroll 4
+        for (int v = tid; v < cu; v += kRingConsumers) {
+          float x[VN];
+          Vec<T>::unpack(v4[v], x);
+          take_vector<VN>(x, e0 + v * VN, bv, bi);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      if (bi >= 0) atomicMax(&s_key[k], make_key(bv, bi));
+    }
+    if (!ok && lane == 0) s_fail = 1;
   }
   __syncthreads();
-  for (int k = warp; k < nb; k += kThreads / 32) {
-    if (!s_last[k]) continue;
-    const long long b = b0 + k;
-    int g = -1;  // lane j: the target's choice of row j of batch row b
-    if (lane < Q) {
-      const unsigned long long key = ld_relaxed_gpu(&A.key[b * Q + lane]);
-      if (key != 0ull) g = static_cast<int>(~static_cast<uint32_t>(key));
-    }
-    const int D = A.D;
-    const int d = lane < D ? A.draft[b * D + lane] : 0;
-    const bool bad_draft = lane < D && (d < 0 || d >= A.V);
-    const bool mismatch = lane < D && (bad_draft || g != d);
-    const unsigned mm = __ballot_sync(0xffffffffu, mismatch);
-    const int a = mm ? __ffs(static_cast<int>(mm)) - 1 : D;
-    const int y = __shfl_sync(0xffffffffu, g, a);
-    const bool bad = bad_draft || (lane < Q && g < 0);
-    if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(A.status, SPECDEC_ERR_INPUT_RANGE);
-    if (lane < Q) A.key[b * Q + lane] = 0ull;  // ready for the next call
-    if (lane == 0) {
-      A.accept_len[b] = a;
-      A.out_token[b] = y;
-      A.ticket[b] = 0u;
-    }
-  }
+  if (s_fail && tid == 0) set_status(A.status, SPECDEC_ERR_TIMEOUT);
+  merge_and_decide<kRingThreads>(A, s_key, s_last, g0, g1, nseg);
 }
 
 struct Geometry {
@@ -268,6 +388,19 @@ Geometry geometry(int B, int D, int V, int vn, int sms) {
   g.units = static_cast<long long>(B) * (D + 1) * g.RU;
   long long G = std::min(2LL * sms, (g.units + kMinUnits - 1) / kMinUnits);
   // A share of at most (kMaxSegs - 2) rows' units touches at most kMaxSegs - 1 rows.
+  G = std::max(G, (g.units + static_cast<long long>(kMaxSegs - 2) * g.RU - 1) /
+                      (static_cast<long long>(kMaxSegs - 2) * g.RU));
+  G = std::max(G, (g.units + kMaxShare - 1) / kMaxShare);
+  g.G = static_cast<int>(std::max(1LL, std::min(G, g.units)));
+  return g;
+}
+
+// The ring kernel's grid: at most one CTA per SM, at least 1024 units (16 KB) per CTA.
+Geometry geometry_ring(int B, int D, int V, int vn, int sms) {
+  Geometry g;
+  g.RU = V / vn;
+  g.units = static_cast<long long>(B) * (D + 1) * g.RU;
+  long long G = std::min<long long>(sms, (g.units + 1023) / 1024);
   G = std::max(G, (g.units + static_cast<long long>(kMaxSegs - 2) * g.RU - 1) /
                       (static_cast<long long>(kMaxSegs - 2) * g.RU));
   G = std::max(G, (g.units + kMaxShare - 1) / kMaxShare);
@@ -289,7 +422,20 @@ int launch(const void* logits, int B, int D, int V, long long row_stride, const 
   const int sms = sm_count();
   if (sms <= 0) return SPECDEC_ERR_CUDA;
   constexpr int VN = kVec ? Vec<T>::N : 1;
-  const Geometry g = geometry(B, D, V, VN, sms);
+  // Rows back to back, whole 16-byte vectors: the bulk-copy ring kernel.
+  const bool use_ring = kVec && row_stride == V && V % VN == 0;
+  if (use_ring) {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPECDEC_ERR_CUDA;
+    if (!attr_set[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          greedy_ring_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+      if (e != cudaSuccess) return map_cuda_error(e);
+      attr_set[dev] = true;
+    }
+  }
+  const Geometry g = use_ring ? geometry_ring(B, D, V, VN, sms) : geometry(B, D, V, VN, sms);
   char* p = static_cast<char*>(ws);
   GreedyArgs A;
   A.logits = logits;
@@ -309,7 +455,10 @@ int launch(const void* logits, int B, int D, int V, long long row_stride, const 
   A.key = reinterpret_cast<unsigned long long*>(p);
   A.ticket = reinterpret_cast<unsigned*>(
       p + round256(static_cast<size_t>(B) * (D + 1) * sizeof(unsigned long long)));
-  greedy_kernel<T, kVec><<<g.G, kThreads, 0, stream>>>(A);
+  if (use_ring)
+    greedy_ring_kernel<T><<<g.G, kRingThreads, kRingBytes, stream>>>(A);
+  else
+    greedy_kernel<T, kVec><<<g.G, kThreads, 0, stream>>>(A);
   return map_cuda_error(cudaGetLastError());
 }
 
