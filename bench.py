@@ -1,11 +1,12 @@
 """Benchmark of the verify + realign hot path (one step = one speculative round).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload vicuna7b|qwen3_8b|glm4_9b]
-                    [--impl specdec|reference] [--copy-engine 0|1]
+                    [--impl specdec|reference] [--copy-engine 0|1] [--ping-pong]
 
 A step is one round: verification of the round's D drafts per row against the target's scores,
-then realignment of the left-padded batch (every layer's surviving K/V columns move to the other
-cache buffer, ids/mask/position IDs are rebuilt).  Inputs are synthetic, seeded and resident on
+then realignment of the left-padded batch (every layer's surviving K/V columns move to their new
+place in the one cache buffer -- rows that do not shift stay -- or, with --ping-pong, to the
+other of two buffers; ids/mask/position IDs are rebuilt).  Inputs are synthetic, seeded and resident on
 the device before the timed region; every round streams gigabytes of K/V, far more than L2.
 With --gpus N (under torchrun) every rank runs an independent replica of the workload (the path
 has no exchange step); ``value`` is the rounds of all ranks over the slowest rank's time.
@@ -37,6 +38,9 @@ def parse():
     p.add_argument("--workload", default="vicuna7b")
     p.add_argument("--impl", default="specdec", choices=["specdec", "reference"])
     p.add_argument("--copy-engine", type=int, default=0)
+    p.add_argument("--ping-pong", action="store_true",
+                   help="two K/V caches, realigned from one into the other (default: one cache "
+                        "realigned in place)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--layers", type=int, default=0,
                    help="override the workload's layer count (smaller cache, e.g. for ncu)")
@@ -193,7 +197,8 @@ def run_specdec(args, rank, ws, local):
     n0 = w.prompt_lengths(gen_cpu)
     prompts = [torch.randint(0, w.V, (int(n),), generator=gen_cpu).tolist() for n in n0]
     cap = w.capacity(int(n0.max()), rounds=R)
-    eng = EqspecBatch(w.layers, w.heads, w.head_dim, w.kv_dtype, w.B, w.D, cap, R, device=dev)
+    eng = EqspecBatch(w.layers, w.heads, w.head_dim, w.kv_dtype, w.B, w.D, cap, R, device=dev,
+                      in_place=not args.ping_pong)
     g = torch.Generator(device=dev).manual_seed(w.seed * 7919 + rank)
     for k in eng.kv:
         k.normal_(generator=g)
@@ -250,7 +255,14 @@ def run_specdec(args, rank, ws, local):
     t_realign = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     n_hist = eng.n_hist.cpu().numpy().astype(np.int64)
     acc = [(n_hist[r + 1] - n_hist[r] - 1) for r in range(Wm, R)]
-    moved_cols = sum(int((n_hist[r + 1] - 1).sum()) for r in range(Wm, R))  # N'_b - 1 per row
+    w_hist = eng.w_hist[:, 0].cpu().numpy().astype(np.int64)
+    moved_cols = 0  # N'_b - 1 per row; in place, rows whose columns do not shift move nothing
+    for r in range(Wm, R):
+        cols = n_hist[r + 1] - 1
+        if not args.ping_pong:
+            shift = (w_hist[r + 1] - n_hist[r + 1]) - (w_hist[r] - n_hist[r])
+            cols = cols[shift != 0]
+        moved_cols += int(cols.sum())
     realign_bytes = 2.0 * moved_cols * w.token_bytes / K
     es = torch.tensor([], dtype=w.logit_dtype).element_size()
     verify_bytes = (w.B * (w.D + 1) * w.V * es + (w.B * w.D * w.V * es if w.mode == "sampled" else 0)
@@ -438,7 +450,7 @@ def run_sweep(args, rank, ws):
         prompts = [torch.randint(0, base.V, (int(n),), generator=gen).tolist() for n in n0]
         cap = int(n0.max()) + R * (base.D + 1) + base.D + 1
         eng = EqspecBatch(base.layers, base.heads, base.head_dim, base.kv_dtype, B, base.D, cap, R,
-                          device=dev)
+                          device=dev, in_place=not args.ping_pong)
         g = torch.Generator(device=dev).manual_seed(B)
         rounds = [synth.greedy_round(g, B, base.D, base.V, 0.7, dtype=base.logit_dtype, device=dev)
                   for _ in range(R)]
@@ -454,7 +466,12 @@ def run_sweep(args, rank, ws):
         ms = [ev[r][0].elapsed_time(ev[r][1]) for r in range(Wm, R)]
         nh = eng.n_hist.cpu().numpy().astype(np.int64)
         wh = eng.w_hist.cpu().numpy().astype(np.int64)[:, 0]
-        alg = [2.0 * (nh[r + 1] - 1).sum() * base.token_bytes for r in range(Wm, R)]
+        def moved(r):  # N'_b - 1 columns per row; in place, rows that do not shift move nothing
+            cols = nh[r + 1] - 1
+            if not args.ping_pong:
+                cols = cols[(wh[r + 1] - nh[r + 1]) - (wh[r] - nh[r]) != 0]
+            return cols.sum()
+        alg = [2.0 * moved(r) * base.token_bytes for r in range(Wm, R)]
         padded = [2.0 * B * (wh[r + 1] - 1) * base.token_bytes for r in range(Wm, R)]
         gbs = sum(alg) / (sum(ms) / 1e3) / 1e9
         out.append({"B": B, "realign_ms_per_round": round(float(np.mean(ms)), 4),
@@ -600,6 +617,7 @@ def main():
                     committed_per_round=res["committed_per_round"], gpu_launches=2 * args.steps,
                     cpu_baseline=cpu)
         line["config"]["cap_cols"] = res["cap_cols"]
+        line["config"]["kv_buffers"] = 2 if args.ping_pong else 1
         print(json.dumps(line))
 
 

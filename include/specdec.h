@@ -224,6 +224,21 @@ typedef struct {
 int specdec_realign(const specdec_realign_args* args, void* stream);
 
 /*
+ * EQSPEC realignment with the K/V cache moved in place: one cache buffer instead of two, which
+ * halves the cache memory.  [BSDDR section 2.2, "shift the KV cache", as an in-place shift.]
+ * Same arguments, results and errors as specdec_realign, except:
+ *   - args->dst must be the same view as args->src (same base, strides, dtype and cap_cols);
+ *     the metadata (ids/mask/pos, lengths, width) is still written to separate outputs;
+ *   - after the call the buffer's columns [W' - N'_b, W' - 1) of row b hold the surviving K/V as
+ *     above; every other column keeps whatever it held before (the old values of columns that
+ *     were not overwritten);
+ *   - rows whose columns do not move (W' - N'_b == W - N_b) are not copied at all.
+ * Each (layer, kv, row, head) run is moved by one CTA in the direction that never overwrites a
+ * source byte before it has been read.
+ */
+int specdec_realign_inplace(const specdec_realign_args* args, void* stream);
+
+/*
  * EXSPEC grouping of a SequencePool by length.  [BSDDR section 2.3: keep a pool of active
  * sequences; group same-length sequences so they need no realignment; only mixed-length ones are
  * realigned.]

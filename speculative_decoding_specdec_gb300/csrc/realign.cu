@@ -21,6 +21,12 @@
 // (completion on an mbarrier) and cp.async.bulk shared->global (bulk groups), keeping
 // stages-1 loads in flight; the other warps meanwhile write the ids, mask and position IDs.
 // Bytes moved = read + write of every surviving column, nothing else.
+//
+// In place (EQSPEC, one K/V buffer): a run moves within its own head row by the row's shift
+// s = dst_col - src_col.  Every run is handled by one CTA (grid shares are rounded down to run
+// starts), which takes its tiles in ascending column order when s < 0 and descending when s > 0;
+// since a tile is stored only after its own load and every earlier load has landed, no store
+// reaches source bytes that are still to be read.  Rows with s = 0 move nothing.
 #include <climits>
 
 #include "common.cuh"
@@ -54,6 +60,7 @@ struct ByteView {
 struct Params {
   ByteView src, dst;
   int mode, R, D, L, H, col_bytes, tile, stages, copy_engine, in_place, by_slot;
+  int kv_in_place;  // EQSPEC: src and dst are one K/V buffer
   int32_t pad_id;
   // EQSPEC
   const int32_t* n_committed;
@@ -152,7 +159,7 @@ __device__ bool build_plan(const Params& p, Plan& s, int* red) {
       const int N = s.aux[r], a = s.acc[r];
       s.src_col[r] = W - N;
       s.dst_col[r] = mx - (N + a + 1);
-      s.ncols[r] = N + a;
+      s.ncols[r] = (p.kv_in_place && s.src_col[r] == s.dst_col[r]) ? 0 : N + a;
     }
   } else if (p.mode == kPoolGather) {
     for (int r = threadIdx.x; r < R; r += kThreads) {
@@ -246,7 +253,8 @@ __device__ __forceinline__ Tile decode(const Params& p, const Plan& s, long long
   const int within = in - s.prefix[r];
   const int c = s.tiles[r];
   const int h = within / c;
-  const int chunk = within - h * c;
+  int chunk = within - h * c;
+  if (p.kv_in_place && s.dst_col[r] > s.src_col[r]) chunk = c - 1 - chunk;  // right shift: last first
   const long long off = static_cast<long long>(chunk) * p.tile;
   const long long run = static_cast<long long>(s.ncols[r]) * p.col_bytes;
   const long long l = g >> 1, kv = g & 1;
@@ -257,6 +265,21 @@ __device__ __forceinline__ Tile decode(const Params& p, const Plan& s, long long
            h * p.dst.shead + static_cast<long long>(s.dst_col[r]) * p.col_bytes + off;
   tl.bytes = static_cast<uint32_t>(min(static_cast<long long>(p.tile), run - off));
   return tl;
+}
+
+// The first tile of the run that holds tile t (t == total: total).
+__device__ long long run_start(const Params& p, const Plan& s, long long t, long long total) {
+  if (t >= total) return total;
+  const int per = s.per_group;
+  const long long g = t / per;
+  const int in = static_cast<int>(t - g * per);
+  int lo = 0, hi = p.R - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s.prefix[mid] <= in) lo = mid; else hi = mid - 1;
+  }
+  const int within = in - s.prefix[lo];
+  return t - within % s.tiles[lo];
 }
 
 // One elected thread moves tiles [t0, t1) through `stages` shared-memory buffers.
@@ -300,7 +323,9 @@ __device__ void copy_bulk(const Params& p, const Plan& s, long long t0, long lon
   bulk_wait_all();
 }
 
-// All threads of the CTA move tiles [t0, t1) with 16-byte loads/stores.
+// All threads of the CTA move tiles [t0, t1) with 16-byte loads/stores.  In place, no byte this
+// kernel writes is read afterwards (tiles go in the shift's direction), so the read-only path
+// stays valid.
 __device__ void copy_vec(const Params& p, const Plan& s, long long t0, long long t1) {
   for (long long t = t0; t < t1; ++t) {
     const Tile tl = decode(p, s, t);
@@ -314,6 +339,9 @@ __device__ void copy_vec(const Params& p, const Plan& s, long long t0, long long
         const int v = base + k * kThreads + threadIdx.x;
         if (v < nv) buf[k] = ldg_stream(src + v);
       }
+      // In place a tile's destination may overlap its own source: every thread has loaded its
+      // part (tiles are at most kThreads * kVecUnroll vectors) before any thread stores.
+      if (p.kv_in_place) __syncthreads();
 #pragma unroll
       for (int k = 0; k < kVecUnroll; ++k) {
         const int v = base + k * kThreads + threadIdx.x;
@@ -415,8 +443,12 @@ __global__ void __launch_bounds__(kThreads) realign_kernel(const Params p) {
 
   const long long total = 2LL * p.L * s.per_group;
   const long long G = gridDim.x;
-  const long long t0 = total * blockIdx.x / G;
-  const long long t1 = total * (blockIdx.x + 1) / G;
+  long long t0 = total * blockIdx.x / G;
+  long long t1 = total * (blockIdx.x + 1) / G;
+  if (p.kv_in_place) {  // whole runs per CTA: round both ends down to the start of their run
+    t0 = run_start(p, s, t0, total);
+    t1 = run_start(p, s, t1, total);
+  }
 
   if (p.copy_engine == 0) {
     if (threadIdx.x == 0) {
@@ -472,6 +504,9 @@ int launch(Params& p, cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return SPECDEC_ERR_CUDA;
   static_assert(SPECDEC_REALIGN_TILE % 16 == 0, "tile must be a multiple of 16 bytes");
+  // The vector engine loads a whole tile before storing it (in place, its destination may
+  // overlap its source): one pass of kThreads * kVecUnroll vectors must cover a tile.
+  static_assert(SPECDEC_REALIGN_TILE <= kThreads * kVecUnroll * 16, "tile larger than one pass");
   static_assert(SPECDEC_REALIGN_STAGES >= 2 && SPECDEC_REALIGN_STAGES <= kMaxStages, "stages");
   p.tile = SPECDEC_REALIGN_TILE;
   p.stages = SPECDEC_REALIGN_STAGES;
@@ -551,8 +586,10 @@ int pool_common(const specdec_pool_args* a, Params& p, bool append) {
 }  // namespace
 }  // namespace specdec
 
-extern "C" int specdec_realign(const specdec_realign_args* a, void* stream) {
-  using namespace specdec;
+namespace specdec {
+namespace {
+
+int realign_common(const specdec_realign_args* a, bool in_place, void* stream) {
   if (!a) return SPECDEC_ERR_INVALID_ARG;
   if (a->B < 0 || a->D < 1) return SPECDEC_ERR_INVALID_ARG;
   if (a->D > SPECDEC_MAX_DRAFT || a->B > kMaxRows) return SPECDEC_ERR_UNSUPPORTED;
@@ -566,10 +603,17 @@ extern "C" int specdec_realign(const specdec_realign_args* a, void* stream) {
   if (s.layers != d.layers || s.heads != d.heads || s.head_dim != d.head_dim || s.rows != a->B ||
       d.rows != a->B)
     return SPECDEC_ERR_INVALID_ARG;
-  uintptr_t slo, shi, dlo, dhi;
-  view_span(s, slo, shi);
-  view_span(d, dlo, dhi);
-  if (slo < dhi && dlo < shi) return SPECDEC_ERR_INVALID_ARG;  // out of place only
+  if (in_place) {  // one K/V buffer: the destination view must be the source view
+    if (d.base != s.base || d.stride_layer != s.stride_layer || d.stride_kv != s.stride_kv ||
+        d.stride_row != s.stride_row || d.stride_head != s.stride_head || d.dtype != s.dtype ||
+        d.cap_cols != s.cap_cols)
+      return SPECDEC_ERR_INVALID_ARG;
+  } else {
+    uintptr_t slo, shi, dlo, dhi;
+    view_span(s, slo, shi);
+    view_span(d, dlo, dhi);
+    if (slo < dhi && dlo < shi) return SPECDEC_ERR_INVALID_ARG;  // out of place: no overlap
+  }
   if (!a->n_committed || !a->width || !a->accept_len || !a->out_token || !a->draft ||
       !a->ids_src || !a->ids_dst || !a->mask_dst || !a->pos_dst || !a->n_committed_dst ||
       !a->width_dst || !a->dev_status)
@@ -602,7 +646,19 @@ extern "C" int specdec_realign(const specdec_realign_args* a, void* stream) {
   p.n_dst = a->n_committed_dst;
   p.width_dst = a->width_dst;
   p.status = a->dev_status;
+  p.kv_in_place = in_place ? 1 : 0;
   return launch(p, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace specdec
+
+extern "C" int specdec_realign(const specdec_realign_args* a, void* stream) {
+  return specdec::realign_common(a, false, stream);
+}
+
+extern "C" int specdec_realign_inplace(const specdec_realign_args* a, void* stream) {
+  return specdec::realign_common(a, true, stream);
 }
 
 extern "C" int specdec_pool_gather(const specdec_pool_args* a, void* stream) {

@@ -34,14 +34,18 @@ class Workspaces:
 
 
 class EqspecBatch:
+    """``in_place=True`` keeps one K/V cache and realigns it in place (half the cache memory);
+    ids, mask and positions stay double-buffered."""
+
     def __init__(self, layers, heads, head_dim, kv_dtype, B, D, cap, max_rounds, device="cuda",
-                 pad_id=0):
+                 pad_id=0, in_place=False):
         self.L, self.H, self.hd, self.B, self.D, self.cap = layers, heads, head_dim, B, D, cap
         self.max_rounds = max_rounds
         self.pad_id = pad_id
         dev = torch.device(device)
+        self.in_place = in_place
         self.kv = [torch.empty((layers, 2, B, heads, cap, head_dim), dtype=kv_dtype, device=dev)
-                   for _ in range(2)]
+                   for _ in range(1 if in_place else 2)]
         self.ids = [torch.full((B, cap), pad_id, dtype=torch.int32, device=dev) for _ in range(2)]
         self.mask = [torch.zeros((B, cap), dtype=torch.uint8, device=dev) for _ in range(2)]
         self.pos = [torch.zeros((B, cap), dtype=torch.int32, device=dev) for _ in range(2)]
@@ -84,7 +88,7 @@ class EqspecBatch:
     # ------------------------------------------------------------------ current state
     @property
     def cache(self):
-        return self.kv[self.cur]
+        return self.kv[0 if self.in_place else self.cur]
 
     @property
     def n_committed(self):
@@ -109,7 +113,8 @@ class EqspecBatch:
         if r >= self.max_rounds:
             raise RuntimeError("round history is full")
         s, d = self.cur, 1 - self.cur
-        specdec.realign(self.kv[s], self.kv[d], self.n_hist[r], self.w_hist[r], self.accept_len,
+        ks, kd = (self.kv[0], self.kv[0]) if self.in_place else (self.kv[s], self.kv[d])
+        specdec.realign(ks, kd, self.n_hist[r], self.w_hist[r], self.accept_len,
                         self.out_token, draft, self.ids[s], self.ids[d], self.mask[d],
                         self.pos[d], self.n_hist[r + 1], self.w_hist[r + 1], self.status,
                         pad_id=self.pad_id, copy_engine=copy_engine, stream=stream)

@@ -72,6 +72,8 @@ lib.specdec_verify_greedy_noalloc.restype = _i
 lib.specdec_verify_greedy_noalloc.argtypes = [_vp, _i, _i, _i, _i, _ll, _vp, _vp, _vp, _vp, _vp]
 lib.specdec_realign.restype = _i
 lib.specdec_realign.argtypes = [ctypes.POINTER(RealignArgs), _vp]
+lib.specdec_realign_inplace.restype = _i
+lib.specdec_realign_inplace.argtypes = [ctypes.POINTER(RealignArgs), _vp]
 lib.specdec_group_by_length.restype = _i
 lib.specdec_group_by_length.argtypes = [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
 lib.specdec_pool_gather.restype = _i
@@ -221,8 +223,11 @@ def verify_sample(target_logits, draft_logits, draft, uniforms, temperature, acc
 def realign(src, dst, n_committed, width, accept_len, out_token, draft, ids_src, ids_dst,
             mask_dst, pos_dst, n_committed_dst, width_dst, status, pad_id=0, copy_engine=0,
             stream=None):
-    """EQSPEC realignment from cache ``src`` into cache ``dst`` (both [L, 2, B, H, cap, hd])."""
+    """EQSPEC realignment from cache ``src`` into cache ``dst`` (both [L, 2, B, H, cap, hd]).
+    Passing the same tensor as ``src`` and ``dst`` moves the K/V in place
+    (specdec_realign_inplace); the metadata outputs stay separate."""
     B, D = draft.shape
+    in_place = src.data_ptr() == dst.data_ptr()
     a = RealignArgs()
     a.src = kv_view(src)
     a.dst = kv_view(dst)
@@ -241,7 +246,11 @@ def realign(src, dst, n_committed, width, accept_len, out_token, draft, ids_src,
     for t, n in ((ids_dst, "ids_dst"), (mask_dst, "mask_dst"), (pos_dst, "pos_dst")):
         if t.shape != (B, dst.shape[4]) or not t.is_contiguous():
             raise ValueError(f"{n} must be a contiguous [B, dst cap] tensor")
-    _check(lib.specdec_realign(ctypes.byref(a), _stream(stream)), "specdec_realign")
+    if in_place:
+        _check(lib.specdec_realign_inplace(ctypes.byref(a), _stream(stream)),
+               "specdec_realign_inplace")
+    else:
+        _check(lib.specdec_realign(ctypes.byref(a), _stream(stream)), "specdec_realign")
 
 
 def group_by_length(lengths, batch_size, max_len, perm, batch_offsets, batch_uniform,

@@ -13,20 +13,23 @@ def host_bits(t):
 
 def eqspec_rounds(L, H, hd, kv_dtype, B, D, V, rounds, prompt_lo, prompt_hi, seed,
                   copy_engine=0, alpha=0.6, logit_dtype=torch.float32, cap_extra=0,
-                  check_full_dst=True):
+                  check_full_dst=True, in_place=False):
     """Greedy verify + realign for ``rounds`` rounds with tagged K/V; every round is compared
     with the oracle: accept lengths, tokens, lengths, width, ids, mask, position IDs, and the
     whole destination cache (the oracle leaves pad columns as they were, and so must the
-    kernel).  Returns the per-round accept lengths."""
+    kernel).  With ``in_place`` the cache is one buffer realigned in place: the expected result
+    is the oracle's realignment into a copy of the source.  Returns the per-round accept
+    lengths."""
     from speculative_decoding_specdec_gb300.engine import EqspecBatch
     gen = synth.make_gen(seed)
     n0 = synth.lengths_uniform(gen, B, prompt_lo, prompt_hi)
     prompts = [torch.randint(0, V, (int(n),), generator=gen).tolist() for n in n0]
     cap = int(n0.max()) + rounds * (D + 1) + D + 1 + cap_extra
-    eng = EqspecBatch(L, H, hd, kv_dtype, B, D, cap, rounds)
+    eng = EqspecBatch(L, H, hd, kv_dtype, B, D, cap, rounds, in_place=in_place)
     W = eng.start(prompts)
     eng.kv[0].fill_(-3.0)
-    eng.kv[1].fill_(-5.0)
+    if not in_place:
+        eng.kv[1].fill_(-5.0)
     toks = [list(p) for p in prompts]
     for b in range(B):
         synth.write_tagged_columns(eng.cache, b, W - len(toks[b]), b,
@@ -41,7 +44,7 @@ def eqspec_rounds(L, H, hd, kv_dtype, B, D, V, rounds, prompt_lo, prompt_hi, see
                                        list(range(len(toks[b]) - 1, len(toks[b]) + D)),
                                        [toks[b][-1]] + draft[b].tolist())
         src = host_bits(eng.cache)
-        dst_before = host_bits(eng.kv[1 - eng.cur])
+        dst_before = src.copy() if in_place else host_bits(eng.kv[1 - eng.cur])
         dd = draft.cuda()
         eng.verify_greedy(logits.cuda(), dd)
         eng.realign(dd, copy_engine=copy_engine)

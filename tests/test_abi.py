@@ -105,6 +105,12 @@ def test_host_validation_codes():
     assert L.specdec_realign(ctypes.byref(a), None) == sd.ERR_UNSUPPORTED
     a.D = 40
     assert L.specdec_realign(ctypes.byref(a), None) == sd.ERR_UNSUPPORTED
+    # in place: the destination must be the source view (checked before any pointer is used)
+    a.D = 4
+    a.src = sd.KvView(4096, 64, 32, 16, 8, sd.BF16, 1, 2, 1, 8, 2)             # 16-byte columns
+    a.dst = sd.KvView(8192, 64, 32, 16, 8, sd.BF16, 1, 2, 1, 8, 2)
+    assert L.specdec_realign_inplace(ctypes.byref(a), None) == sd.ERR_INVALID_ARG
+    assert L.specdec_realign_inplace(None, None) == sd.ERR_INVALID_ARG
     # grouping
     assert L.specdec_group_by_length(None, -1, 8, 10, None, None, None, None, None, None, None) == sd.ERR_INVALID_ARG
     assert L.specdec_group_by_length(None, 5000, 8, 10, None, None, None, None, None, None, None) == sd.ERR_UNSUPPORTED

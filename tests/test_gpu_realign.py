@@ -42,6 +42,44 @@ def test_shapes(B, D, lo, hi, hd, dtype):
                   seed=B + D, alpha=0.6)
 
 
+@pytest.mark.parametrize("B,D,lo,hi,hd,dtype,L,H", [
+    (2, 4, 5, 20, 64, torch.float32, 1, 2),      # tiny
+    (8, 5, 20, 300, 128, torch.bfloat16, 2, 4),  # multi-tile runs, ragged last tiles
+    (64, 3, 1, 12, 64, torch.bfloat16, 2, 2),    # many short rows: zero-shift and one-column runs
+    (3, 31, 2, 100, 8, torch.bfloat16, 2, 2),    # D = 31, 16-byte columns
+    (300, 2, 1, 6, 64, torch.float32, 2, 2),     # more rows than one CTA's threads
+])
+def test_in_place(B, D, lo, hi, hd, dtype, L, H):
+    """The whole buffer after an in-place realignment equals the oracle's realignment into a
+    copy of the source: surviving columns moved, every other column untouched."""
+    eqspec_rounds(L, H, hd, dtype, B=B, D=D, V=300, rounds=4, prompt_lo=lo, prompt_hi=hi,
+                  seed=50 + B + D, alpha=0.6, in_place=True)
+
+
+def test_in_place_long_shifts():
+    # prompts of very different lengths: shifts of hundreds of columns both ways over rounds
+    eqspec_rounds(2, 2, 128, torch.bfloat16, B=6, D=6, V=200, rounds=5, prompt_lo=1,
+                  prompt_hi=700, seed=77, alpha=0.9, in_place=True)
+
+
+def test_in_place_rejects_a_different_destination():
+    import speculative_decoding_specdec_gb300.specdec as sd
+    buf = _one_round_buffers()
+    a = sd.RealignArgs()
+    a.src = sd.kv_view(buf["kv"][0])
+    a.dst = sd.kv_view(buf["kv"][1])
+    a.B, a.D = 4, 3
+    for name, key in (("n_committed", "n"), ("width", "w"), ("accept_len", "a"), ("out_token", "y"),
+                      ("draft", "d"), ("ids_src", None), ("ids_dst", None), ("pos_dst", "pos"),
+                      ("n_committed_dst", "n2"), ("width_dst", "w2"), ("dev_status", "st")):
+        t = buf["ids"][0] if name == "ids_src" else buf["ids"][1] if name == "ids_dst" else buf[key]
+        setattr(a, name, t.data_ptr())
+    a.mask_dst = buf["mask"].data_ptr()
+    assert sd.lib.specdec_realign_inplace(sd.ctypes.byref(a), None) == sd.ERR_INVALID_ARG
+    a.dst = sd.kv_view(buf["kv"][0])
+    assert sd.lib.specdec_realign(sd.ctypes.byref(a), None) == sd.ERR_INVALID_ARG  # overlap
+
+
 def test_all_rows_accept_everything():
     eqspec_rounds(1, 3, 64, torch.bfloat16, B=6, D=4, V=200, rounds=3, prompt_lo=10,
                   prompt_hi=90, seed=7, alpha=1.0)
@@ -98,8 +136,11 @@ def test_range_errors_write_nothing(bad):
 def test_host_errors():
     import speculative_decoding_specdec_gb300.specdec as sd
     buf = _one_round_buffers()
-    with pytest.raises(sd.SpecdecError):                    # same buffer in and out
-        _call(buf, kv=[buf["kv"][0], buf["kv"][0]])
+    kv0 = buf["kv"][0]
+    n, hd = kv0.numel(), kv0.shape[-1]
+    big = torch.zeros(n + hd, dtype=kv0.dtype, device=kv0.device)
+    with pytest.raises(sd.SpecdecError):                    # overlapping, not the same view
+        _call(buf, kv=[big[:n].view(kv0.shape), big[hd:].view(kv0.shape)])
     with pytest.raises(sd.SpecdecError):                    # lengths aliasing
         _call(buf, n2=buf["n"])
     odd = torch.zeros(1, 2, 4, 2, 40, 4, dtype=torch.bfloat16, device="cuda")   # 8-byte columns
@@ -117,16 +158,19 @@ FULL = {
 }
 
 
+@pytest.mark.parametrize("in_place", [False, True])
 @pytest.mark.parametrize("name", list(FULL))
-def test_full_size_rounds(name):
-    """Three rounds at the full cache size (capacity for the workload's full round count)."""
+def test_full_size_rounds(name, in_place):
+    """Three rounds at the full cache size (capacity for the workload's full round count), with
+    two cache buffers or one realigned in place."""
     from speculative_decoding_specdec_gb300.engine import EqspecBatch
     c = FULL[name]
     w = synth.WORKLOADS[name]
     gen = synth.make_gen(50 + w.seed)
     n0 = w.prompt_lengths(gen)
     cap = w.capacity(int(n0.max()))
-    eng = EqspecBatch(c["L"], c["H"], 128, torch.bfloat16, c["B"], c["D"], cap, 3)
+    eng = EqspecBatch(c["L"], c["H"], 128, torch.bfloat16, c["B"], c["D"], cap, 3,
+                      in_place=in_place)
     prompts = [torch.randint(0, c["V"], (int(n),), generator=gen).tolist() for n in n0]
     W = eng.start(prompts)
     g = torch.Generator(device="cuda").manual_seed(1)
@@ -138,13 +182,13 @@ def test_full_size_rounds(name):
     for _ in range(3):
         logits, draft = synth.greedy_round(gen, c["B"], c["D"], c["V"], c["alpha"],
                                            dtype=torch.bfloat16)
-        src = eng.cache
+        src = eng.cache.clone() if in_place else eng.cache   # the in-place move overwrites it
         dd = draft.cuda()
         eng.verify_greedy(logits.cuda(), dd)
         planes = [(int(rng.integers(c["L"])), int(rng.integers(2))) for _ in range(2)]
         src_planes = [src[l, kv].view(torch.int16).cpu().numpy() for l, kv in planes]
-        dst_planes = [eng.kv[1 - eng.cur][l, kv].view(torch.int16).cpu().numpy()
-                      for l, kv in planes]
+        dst_planes = [(src if in_place else eng.kv[1 - eng.cur])[l, kv].view(torch.int16)
+                      .cpu().numpy() for l, kv in planes]
         eng.realign(dd)
         torch.cuda.synchronize()
         assert int(eng.status.item()) == 0
