@@ -98,8 +98,51 @@ def sum_over_ranks(x: float, ws: int) -> float:
 
 # ------------------------------------------------------------------------------ clocks
 
+class NvmlClocks:
+    """Read-only NVML queries through ctypes (SM clock, its maximum, clock-event reasons) for the
+    device with the given UUID; ``ok`` is False when NVML cannot be used."""
+    # clock-event reason bits of NVML's nvmlClocksEventReasons
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, uuid):
+        import ctypes
+        self.ok = False
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            if uuid is None or self.lib.nvmlDeviceGetHandleByUUID(
+                    uuid.encode(), ctypes.byref(self.handle)) != 0:
+                return
+            self.u = ctypes.c_uint()
+            self.ull = ctypes.c_ulonglong()
+            self.ctypes = ctypes
+            self.ok = self.max_sm() is not None
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def sm(self):
+        return (self.u.value if self.lib.nvmlDeviceGetClockInfo(
+            self.handle, 1, self.ctypes.byref(self.u)) == 0 else None)  # 1: NVML_CLOCK_SM
+
+    def max_sm(self):
+        return (self.u.value if self.lib.nvmlDeviceGetMaxClockInfo(
+            self.handle, 1, self.ctypes.byref(self.u)) == 0 else None)
+
+    def reasons(self):
+        f = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        if f(self.handle, self.ctypes.byref(self.ull)) != 0:
+            return set()
+        return {name for name, bit in self.BITS.items() if self.ull.value & bit}
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """SM clock and clock-event reasons sampled while the timed region runs: an NVML thread polling
+    back to back (timed regions can be a few ms long), else nvidia-smi every 10 ms (started
+    before the region, which begins once its first sample is in)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -107,18 +150,48 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.lines = []
+        self.nv_samples = []
+        self.nv_max = None
+        self.nv = None
+
+    def _poll(self):  # back to back: each NVML query already takes on the order of 1 ms
+        while not self.stop.is_set():
+            mhz = self.nv.sm()
+            if mhz is not None:
+                self.nv_samples.append((mhz, self.nv.reasons()))
 
     def __enter__(self):
+        import threading
+        import torch
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except (AttributeError, RuntimeError):
+            uuid = None
+        self.nv = NvmlClocks(uuid)
+        if self.nv.ok:
+            self.nv_max = self.nv.max_sm()
+            self.stop = threading.Event()
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            first = self.proc.stdout.readline()  # the region starts once sampling runs
+            if first.strip():
+                self.lines.append(first)
         except OSError:
             self.proc = None
         return self
 
     def __exit__(self, *exc):
+        if self.nv is not None and self.nv.ok:
+            self.stop.set()
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -126,11 +199,14 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
-        else:
-            self.lines = []
+            self.lines += [ln for ln in out.splitlines() if ln.strip()]
 
     def summary(self):
+        if self.nv_samples:
+            sm = [m for m, _ in self.nv_samples]
+            reasons = set().union(*(r for _, r in self.nv_samples))
+            return {"sm_mhz": statistics.median(sm), "sm_max_mhz": self.nv_max,
+                    "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
@@ -146,7 +222,7 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi"}
 
 
 def captured_traffic(kernel: str, algorithmic_bytes: float):
