@@ -33,6 +33,13 @@ Readings where the pages leave a step open (each is listed again in the design doc):
 * A draft x is accepted iff u < p(x)/q(x) with u uniform in [0, 1); this is the min(1, p/q) rule
   with the min implicit.  u == p/q rejects.
 * Temperature T divides the scores of both models ("same sampling settings" [IE5, Exactness]).
+* Top-k / top-p, the other sampling settings the pages name ("temperature and top-p" [IE5, Draft
+  Possible Tokens]), apply to both models' rows alike.  A row's tokens are ordered by score,
+  highest first, ties by lower token index.  Top-k (1 <= k < V; otherwise off) keeps the first k.
+  Top-p (0 < top_p < 1; 1 is off) then keeps, in the same order, every token whose preceding
+  probability mass within the kept set (renormalised) is below top_p, so the token that reaches
+  top_p is kept.  p and q are the softmax at T restricted to their kept sets and renormalised;
+  acceptance, residual and bonus use them as they are.
 * The replacement or bonus token is an inverse-CDF draw with the row's last uniform u[b][D], over
   token ids in ascending order, first k whose running sum exceeds u * (total).  If the residual
   max(0, p - q) is all zero the draw falls back to p.
@@ -56,6 +63,9 @@ __all__ = [
     "greedy_choice",
     "verify_greedy",
     "softmax",
+    "sampling_keep",
+    "filtered_softmax",
+    "top_p_margin",
     "verify_sample",
     "realign_plan",
     "realign",
@@ -132,6 +142,55 @@ def softmax(scores, temperature: float):
     return e / e.sum()
 
 
+def _sort_order(z):
+    """Token order of the sampling settings: score descending, lower index first on ties."""
+    return np.lexsort((np.arange(len(z)), -z))
+
+
+def sampling_keep(scores, temperature: float, top_k: int = 0, top_p: float = 1.0):
+    """Boolean mask of the tokens one score row keeps under top-k and top-p (module readings)."""
+    z = np.asarray(scores, dtype=np.float64)
+    V = len(z)
+    if not 0.0 < top_p <= 1.0:
+        raise OracleError("top_p")
+    order = _sort_order(z)
+    k = V if (top_k <= 0 or top_k >= V) else int(top_k)
+    kept = order[:k]
+    if top_p < 1.0:
+        p = softmax(z[kept], temperature)              # renormalised over the top-k set
+        before = np.concatenate(([0.0], np.cumsum(p)[:-1]))
+        kept = kept[before < top_p]
+    keep = np.zeros(V, dtype=bool)
+    keep[kept] = True
+    return keep
+
+
+def filtered_softmax(scores, temperature: float, top_k: int = 0, top_p: float = 1.0):
+    """Softmax at T restricted to the kept tokens and renormalised (plain softmax when both
+    settings are off)."""
+    z = np.asarray(scores, dtype=np.float64)
+    if (top_k <= 0 or top_k >= len(z)) and top_p >= 1.0:
+        return softmax(z, temperature)
+    p = softmax(z, temperature) * sampling_keep(z, temperature, top_k, top_p)
+    return p / p.sum()
+
+
+def top_p_margin(scores, temperature: float, top_k: int = 0, top_p: float = 1.0):
+    """How far top_p lies from the nearest cumulative mass at which the top-p cut would move
+    (the preceding mass of the last kept and of the first dropped token); inf when top-p is off.
+    A top-p cut computed in lower precision can differ from this oracle's only where this margin
+    is below that precision."""
+    z = np.asarray(scores, dtype=np.float64)
+    if top_p >= 1.0:
+        return np.inf
+    order = _sort_order(z)
+    V = len(z)
+    k = V if (top_k <= 0 or top_k >= V) else int(top_k)
+    p = softmax(z[order[:k]], temperature)
+    before = np.concatenate(([0.0], np.cumsum(p)[:-1]))
+    return float(np.min(np.abs(before - top_p)))
+
+
 def _inverse_cdf(weights, u: float):
     """First k (ascending token id) whose running sum exceeds u * total; the running sum is
     sequential.  If rounding leaves no such k, the last k with a nonzero weight."""
@@ -145,7 +204,8 @@ def _inverse_cdf(weights, u: float):
     return k, t, total, lo, cdf[k]
 
 
-def verify_sample(target_logits, draft_logits, draft, uniforms, temperature: float):
+def verify_sample(target_logits, draft_logits, draft, uniforms, temperature: float,
+                  top_k: int = 0, top_p: float = 1.0):
     """Speculative rejection sampling over a batch.
 
     target_logits: [B, D+1, V] scores of the main model (p after softmax at T).
@@ -156,6 +216,9 @@ def verify_sample(target_logits, draft_logits, draft, uniforms, temperature: flo
     For j = 0..D-1 (left to right): accept d_{j+1} iff u[b][j] < p_j(d)/q_j(d), i.e. with
     probability min(1, p/q).  At the first rejection j*: draw y from normalize(max(0, p_j* - q_j*)).
     If every draft is accepted: draw the bonus y from p_D.
+    With top_k / top_p set, p and q are the filtered, renormalised distributions of every row
+    (filtered_softmax); a draft outside q's kept set (q(d) = 0) is accepted, one outside p's kept
+    set only is rejected.
 
     Returns (accept_len[B], out_token[B], residual[B, V], trace) where residual[b] is the
     normalised distribution y_b was drawn from, and trace holds float64 diagnostics for the
@@ -185,8 +248,8 @@ def verify_sample(target_logits, draft_logits, draft, uniforms, temperature: flo
     for b in range(B):
         a = D
         for j in range(D):
-            p = softmax(tl[b, j], temperature)
-            q = softmax(dl[b, j], temperature)
+            p = filtered_softmax(tl[b, j], temperature, top_k, top_p)
+            q = filtered_softmax(dl[b, j], temperature, top_k, top_p)
             x = int(draft[b, j])
             r = p[x] / q[x] if q[x] > 0 else np.inf
             ratio[b, j] = r
@@ -194,13 +257,13 @@ def verify_sample(target_logits, draft_logits, draft, uniforms, temperature: flo
                 a = j
                 break
         if a < D:
-            p = softmax(tl[b, a], temperature)
-            q = softmax(dl[b, a], temperature)
+            p = filtered_softmax(tl[b, a], temperature, top_k, top_p)
+            q = filtered_softmax(dl[b, a], temperature, top_k, top_p)
             w = np.maximum(0.0, p - q)   # the probability still missing for each token
             if not (w > 0).any():
                 w = p                    # unreachable unless p == q exactly
         else:
-            w = softmax(tl[b, D], temperature)   # bonus: distribution after the full draft
+            w = filtered_softmax(tl[b, D], temperature, top_k, top_p)  # bonus: after the full draft
         k, t, total, lo, hi = _inverse_cdf(w, u[b, D])
         accept_len[b] = a
         out_token[b] = k
