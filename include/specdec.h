@@ -144,6 +144,10 @@ int specdec_verify_greedy_noalloc(const void* logits, int dtype, int B, int D, i
  *   residual_out  [B][V] float32 out, may be NULL: the normalised distribution y_b was drawn from
  *                 (normalize(max(0, p_a - q_a)) after a rejection at a = a_b < D, p_D when all
  *                 drafts were accepted).
+ *   keep_bounds   [B][2D+1] specdec_keep_bound from specdec_sampling_filter (rows 0..D the
+ *                 target's, D+1..2D the draft's), or NULL for no top-k / top-p: p_j and q_j are
+ *                 then the softmax restricted to each row's kept tokens and renormalised.  A draft
+ *                 outside q's kept set is accepted; outside p's only, rejected.
  * The draw is an inverse CDF over ascending token ids: the first k whose running sum exceeds
  * u[b][D] * (total).  If max(0, p - q) is zero everywhere the draw uses p instead.
  * Precision: exponentials and per-element probabilities in fp32; the acceptance ratio p(d)/q(d)
@@ -154,8 +158,42 @@ int specdec_verify_greedy_noalloc(const void* logits, int dtype, int B, int D, i
 int specdec_verify_sample(const void* target_logits, const void* draft_logits, int dtype, int B,
                           int D, int V, long long row_stride, float temperature,
                           const int32_t* draft, const float* uniforms, int32_t* accept_len,
-                          int32_t* out_token, float* residual_out, int32_t* dev_status,
-                          void* stream);
+                          int32_t* out_token, float* residual_out, const void* keep_bounds,
+                          int32_t* dev_status, void* stream);
+
+/*
+ * The kept set of one score row under the sampling settings, as its last token in the settings'
+ * order.  A token with score x at index v is kept iff key(x) > key, or key(x) == key and
+ * v <= index, where key(x) is the order-preserving code of the score as a float: its IEEE bits
+ * with -0 taken as +0, the sign bit set for x >= 0 and all bits inverted for x < 0.
+ */
+typedef struct {
+  uint32_t key;
+  int32_t index;
+} specdec_keep_bound;
+
+/*
+ * Top-k / top-p keep bounds of every score row, for specdec_verify_sample.  [IE5, "Draft Possible
+ * Tokens, Then Verify Them Together": sampling settings "such as temperature and top-p";
+ * "Exactness Means Different Things For Greedy And Sampled Output": both models use the same
+ * sampling settings.]
+ *
+ * Reading: a row's tokens are ordered by score, highest first, ties by lower token index.
+ * top_k (1 <= top_k < V; 0 or >= V is off) keeps the first top_k tokens; top_p (0 < top_p < 1;
+ * 1 is off) then keeps, in the same order, every token whose preceding probability mass (softmax
+ * at T within the kept set) is below top_p, so the token that reaches top_p is kept.
+ *   target_logits, draft_logits, dtype, B, D, V, row_stride, temperature  as for
+ *                 specdec_verify_sample.
+ *   keep_bounds   [B][2D+1] specdec_keep_bound out (8-byte aligned device memory).
+ * Top-k is exact.  Top-p sums the masses 2^(x*log2(e)/T - o) in 64-bit fixed point (2^-44 of the
+ * row's largest mass, from an exp2 with relative error below 2^-21): its cut can differ from an
+ * exact one only where top_p lies within about 1e-6 of a cumulative mass of the order.  Rows with
+ * NaN or +inf scores keep every token (verification reports them).  Limits: as for
+ * specdec_verify_sample; top_k >= 0, 0 < top_p <= 1.
+ */
+int specdec_sampling_filter(const void* target_logits, const void* draft_logits, int dtype, int B,
+                            int D, int V, long long row_stride, float temperature, int top_k,
+                            float top_p, void* keep_bounds, int32_t* dev_status, void* stream);
 
 /*
  * A view of a K/V cache in device memory.  Element (layer l, k-or-v kv, row r, head h,

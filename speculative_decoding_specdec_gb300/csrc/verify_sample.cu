@@ -207,8 +207,20 @@ struct SampleArgs {
   int32_t* accept_len;
   int32_t* out_token;
   float* residual;
+  const uint2* keep;  // [B][2D+1] keep bounds of the sampling settings, or NULL (keep all)
   int32_t* status;
 };
+
+// Order-preserving code of a float score (-0 counted as +0), and the keep test of a token with
+// score x at index v against its row's bound (key, index).
+__device__ __forceinline__ uint32_t score_key(float f) {
+  const uint32_t u = (f == 0.f) ? 0u : __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ bool kept(uint2 bd, float x, int v) {
+  const uint32_t k = score_key(x);
+  return k > bd.x || (k == bd.x && v <= static_cast<int>(bd.y));
+}
 
 template <typename T, bool kVec, int W>
 __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kernel(const SampleArgs A) {
@@ -231,6 +243,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
   __shared__ int s_a, s_bad, s_found, s_y, s_last, s_fail;
   __shared__ __align__(8) uint64_t full[kMaxRingStages], empty[kMaxRingStages], pbar;
   __shared__ StreamPlan plan;
+  __shared__ uint2 s_keep[kMaxQ];            // the rows' keep bounds (sampling settings)
   __shared__ int pre_d[SPECDEC_MAX_DRAFT];   // fetched while the slice streams
   __shared__ float pre_u[SPECDEC_MAX_DRAFT + 1], pre_z[SPECDEC_MAX_DRAFT], pre_w[SPECDEC_MAX_DRAFT];
 
@@ -277,6 +290,9 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
     (&po[0][0])[k] = kOffsetNone;
     (&ps[0][0])[k] = 0.f;
   }
+  const bool filter = A.keep != nullptr;
+  for (int k = tid; k < Q; k += kThreads)
+    s_keep[k] = filter ? A.keep[static_cast<long long>(b) * Q + k] : make_uint2(0u, 0x7fffffffu);
   if (tid == 0) {
     s_bad = 0;
     s_found = 0;
@@ -329,7 +345,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
       int cur = -1;
       float o = kOffsetNone, s = 0.f;
       const bool ok = stream_consume(
-          plan, dyn, full, empty, [&](int q, int, int n, const char* stage) {  // row segment
+          plan, dyn, full, empty, [&](int q, int v0, int n, const char* stage) {  // row segment
             if (q != cur) {
               if (cur >= 0) {
                 warp_merge(o, s);
@@ -342,6 +358,18 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
             const uint4* v4 = reinterpret_cast<const uint4*>(stage);
             const int nv = n / VN;
             int v = tid;
+            if (filter) {  // sampling settings: tokens outside the row's kept set weigh 0
+              const uint2 bd = s_keep[q];
+              for (; v < nv; v += kConsumers) {
+                float x[VN];
+                Vec<T>::unpack(v4[v], x);
+#pragma unroll
+                for (int i = 0; i < VN; ++i)
+                  if (!kept(bd, x[i], v0 + v * VN + i)) x[i] = kNegInf;
+                fold<VN>(x, c2, o, s);
+              }
+              return;
+            }
             for (; v + 3 * kConsumers < nv; v += 4 * kConsumers) {
               uint4 r[4];
 #pragma unroll
@@ -368,7 +396,8 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
       const T* row = row_ptr(q);
       float o = kOffsetNone, s = 0.f;
       for (int e = s0 + tid; e < s1; e += kConsumers) {
-        const float x = Vec<T>::scalar(row + e);
+        float x = Vec<T>::scalar(row + e);
+        if (!kept(s_keep[q], x, e)) x = kNegInf;
         fold<1>(&x, c2, o, s);
       }
       warp_merge(o, s);
@@ -383,7 +412,8 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
     if (lane == kWarps && kVec) {  // elements past the streamed body (fewer than one vector)
       const T* row = row_ptr(q);
       for (int e = tail_from; e < s1; ++e) {
-        const float x = Vec<T>::scalar(row + e);
+        float x = Vec<T>::scalar(row + e);
+        if (!kept(s_keep[q], x, e)) x = kNegInf;
         fold<1>(&x, c2, o, s);
       }
     }
@@ -422,8 +452,9 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
         bad = true;
         accept = false;
       } else {
-        const float z = pre_z[lane];
-        const float w = pre_w[lane];
+        // A draft outside a row's kept set has probability 0 there.
+        const float z = kept(s_keep[lane], pre_z[lane], d) ? pre_z[lane] : kNegInf;
+        const float w = kept(s_keep[D + 1 + lane], pre_w[lane], d) ? pre_w[lane] : kNegInf;
         if (w == kNegInf) {
           accept = true;  // q(d) = 0
         } else {
@@ -504,20 +535,31 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
   const float ow = resid ? go[D + 1 + a] : 0.f;
   const float iw = s_iw;
   bool use_p = !resid;
+  const uint2 kz = s_keep[a], kw = s_keep[resid ? D + 1 + a : a];
+  auto zmask = [&](float x, int i) { return kept(kz, x, s0 + i) ? x : kNegInf; };
+  auto wmask = [&](float x, int i) { return kept(kw, x, s0 + i) ? x : kNegInf; };
   auto r_at = [&](int i) -> float {
-    const float p = ex2(fmaf(Vec<T>::scalar(zs + i), c2, -oz)) * iz;
+    const float p = ex2(fmaf(zmask(Vec<T>::scalar(zs + i), i), c2, -oz)) * iz;
     if (use_p) return p;
-    return fmaxf(0.f, p - ex2(fmaf(Vec<T>::scalar(ws + i), c2, -ow)) * iw);
+    return fmaxf(0.f, p - ex2(fmaf(wmask(Vec<T>::scalar(ws + i), i), c2, -ow)) * iw);
   };
   // The VN residual values of elements [i, i + VN) (i a multiple of VN, inside the slice).
   auto r_vec = [&](int i, float* r) {
     float z[VN];
     Vec<T>::unpack(*reinterpret_cast<const uint4*>(zs + i), z);
+    if (filter) {
+#pragma unroll
+      for (int k = 0; k < VN; ++k) z[k] = zmask(z[k], i + k);
+    }
 #pragma unroll
     for (int k = 0; k < VN; ++k) r[k] = ex2(fmaf(z[k], c2, -oz)) * iz;
     if (!use_p) {
       float w[VN];
       Vec<T>::unpack(*reinterpret_cast<const uint4*>(ws + i), w);
+      if (filter) {
+#pragma unroll
+        for (int k = 0; k < VN; ++k) w[k] = wmask(w[k], i + k);
+      }
 #pragma unroll
       for (int k = 0; k < VN; ++k) r[k] = fmaxf(0.f, r[k] - ex2(fmaf(w[k], c2, -ow)) * iw);
     }
@@ -740,8 +782,8 @@ extern "C" int specdec_verify_sample(const void* target_logits, const void* draf
                                      int dtype, int B, int D, int V, long long row_stride,
                                      float temperature, const int32_t* draft,
                                      const float* uniforms, int32_t* accept_len,
-                                     int32_t* out_token, float* residual_out, int32_t* dev_status,
-                                     void* stream) {
+                                     int32_t* out_token, float* residual_out,
+                                     const void* keep_bounds, int32_t* dev_status, void* stream) {
   using namespace specdec;
   const int es = elem_size(dtype);
   if (es == 0 || B < 0 || D < 1 || V < 1 || row_stride < V) return SPECDEC_ERR_INVALID_ARG;
@@ -759,8 +801,10 @@ extern "C" int specdec_verify_sample(const void* target_logits, const void* draf
   const bool vec = reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&
                    reinterpret_cast<uintptr_t>(draft_logits) % 16 == 0 &&
                    (row_stride * es) % 16 == 0;
+  if (reinterpret_cast<uintptr_t>(keep_bounds) % 8) return SPECDEC_ERR_INVALID_ARG;
   SampleArgs A = {target_logits, draft_logits, D, V, row_stride, temperature, 1, V, draft,
-                  uniforms, accept_len, out_token, residual_out, dev_status};
+                  uniforms, accept_len, out_token, residual_out,
+                  static_cast<const uint2*>(keep_bounds), dev_status};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SPECDEC_BF16)
     return vec ? launch<uint16_t, true>(A, B, s) : launch<uint16_t, false>(A, B, s);

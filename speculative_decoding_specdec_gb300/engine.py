@@ -32,6 +32,16 @@ class Workspaces:
         B, D = draft.shape
         return self.get("greedy", specdec.greedy_workspace_bytes(B, D))
 
+    def bounds(self, draft):
+        """Keep-bound buffer [B, 2D+1, 2] int32 for the sampling settings."""
+        B, D = draft.shape
+        key = ("bounds", B, D)
+        t = self._ws.get(key)
+        if t is None:
+            t = torch.zeros((B, 2 * D + 1, 2), dtype=torch.int32, device=self.device)
+            self._ws[key] = t
+        return t
+
 
 class EqspecBatch:
     """``in_place=True`` keeps one K/V cache and realigns it in place (half the cache memory);
@@ -104,9 +114,17 @@ class EqspecBatch:
                               self.workspaces.greedy(logits, draft), stream)
 
     def verify_sample(self, target_logits, draft_logits, draft, uniforms, temperature,
-                      residual=None, stream=None):
+                      residual=None, stream=None, top_k=0, top_p=1.0):
+        """Sampled verification; with top_k / top_p the rows' keep bounds are computed first
+        (specdec_sampling_filter) into a buffer this batch keeps."""
+        bounds = None
+        if (0 < top_k < target_logits.shape[-1]) or top_p < 1.0:
+            bounds = self.workspaces.bounds(draft)
+            specdec.sampling_filter(target_logits, draft_logits, temperature, top_k, top_p,
+                                    bounds, self.status, stream)
         specdec.verify_sample(target_logits, draft_logits, draft, uniforms, temperature,
-                              self.accept_len, self.out_token, self.status, residual, stream)
+                              self.accept_len, self.out_token, self.status, residual, stream,
+                              keep_bounds=bounds)
 
     def realign(self, draft, copy_engine=0, stream=None):
         r = self.round

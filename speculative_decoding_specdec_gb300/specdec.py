@@ -83,7 +83,14 @@ lib.specdec_pool_append.argtypes = [ctypes.POINTER(PoolArgs), _vp]
 if hasattr(lib, "specdec_verify_sample"):
     lib.specdec_verify_sample.restype = _i
     lib.specdec_verify_sample.argtypes = [_vp, _vp, _i, _i, _i, _i, _ll, _f, _vp, _vp, _vp, _vp,
-                                          _vp, _vp, _vp]
+                                          _vp, _vp, _vp, _vp]
+lib.specdec_sampling_filter.restype = _i
+lib.specdec_sampling_filter.argtypes = [_vp, _vp, _i, _i, _i, _i, _ll, _f, _i, _f, _vp, _vp, _vp]
+
+
+class KeepBound(ctypes.Structure):
+    """specdec_keep_bound: the last kept token of a row under the sampling settings."""
+    _fields_ = [("key", ctypes.c_uint32), ("index", ctypes.c_int32)]
 
 
 class SpecdecError(RuntimeError):
@@ -197,9 +204,32 @@ def verify_greedy_noalloc(logits, draft, accept_len, out_token, status, stream=N
            "specdec_verify_greedy_noalloc")
 
 
+def sampling_filter(target_logits, draft_logits, temperature, top_k, top_p, keep_bounds, status,
+                    stream=None):
+    """Top-k / top-p keep bounds of every score row into ``keep_bounds``, an int32 CUDA tensor
+    [B, 2D+1, 2] holding specdec_keep_bound (key bits, index) per row."""
+    B, Dp1 = target_logits.shape[0], target_logits.shape[1]
+    D = Dp1 - 1
+    V = target_logits.shape[-1]
+    rs = _score_rows(target_logits, B, D + 1, "target_logits")
+    rs2 = _score_rows(draft_logits, B, D, "draft_logits")
+    if rs != rs2 or draft_logits.dtype != target_logits.dtype or draft_logits.shape[-1] != V:
+        raise ValueError("target and draft scores must share dtype, V and row stride")
+    _need(keep_bounds, torch.int32, "keep_bounds")
+    _need(status, torch.int32, "status")
+    if tuple(keep_bounds.shape) != (B, 2 * D + 1, 2) or not keep_bounds.is_contiguous():
+        raise ValueError("keep_bounds must be a contiguous [B, 2D+1, 2] int32 tensor")
+    _check(lib.specdec_sampling_filter(_ptr(target_logits), _ptr(draft_logits),
+                                       dtype_code(target_logits.dtype), B, D, V, rs,
+                                       float(temperature), int(top_k), float(top_p),
+                                       _ptr(keep_bounds), _ptr(status), _stream(stream)),
+           "specdec_sampling_filter")
+
+
 def verify_sample(target_logits, draft_logits, draft, uniforms, temperature, accept_len,
-                  out_token, status, residual=None, stream=None):
-    """Sampled verification (min(1, p/q) acceptance, normalised max(0, p - q) residual draw)."""
+                  out_token, status, residual=None, stream=None, keep_bounds=None):
+    """Sampled verification (min(1, p/q) acceptance, normalised max(0, p - q) residual draw);
+    ``keep_bounds`` from sampling_filter applies top-k / top-p."""
     B, D = draft.shape
     V = target_logits.shape[-1]
     rs = _score_rows(target_logits, B, D + 1, "target_logits")
@@ -217,7 +247,8 @@ def verify_sample(target_logits, draft_logits, draft, uniforms, temperature, acc
                                      dtype_code(target_logits.dtype), B, D, V, rs,
                                      float(temperature), _ptr(draft), _ptr(uniforms),
                                      _ptr(accept_len), _ptr(out_token), _ptr(residual),
-                                     _ptr(status), _stream(stream)), "specdec_verify_sample")
+                                     _ptr(keep_bounds), _ptr(status), _stream(stream)),
+           "specdec_verify_sample")
 
 
 def realign(src, dst, n_committed, width, accept_len, out_token, draft, ids_src, ids_dst,

@@ -50,6 +50,7 @@ int main(void) {
   printf("specdec_kv_view %zu\n", sizeof(specdec_kv_view));
   printf("specdec_realign_args %zu\n", sizeof(specdec_realign_args));
   printf("specdec_pool_args %zu\n", sizeof(specdec_pool_args));
+  printf("specdec_keep_bound %zu\n", sizeof(specdec_keep_bound));
   %FIELDS%
   return 0;
 }
@@ -59,7 +60,7 @@ int main(void) {
 def test_ctypes_layout_matches_c(tmp_path):
     import speculative_decoding_specdec_gb300.specdec as sd
     structs = {"specdec_kv_view": sd.KvView, "specdec_realign_args": sd.RealignArgs,
-               "specdec_pool_args": sd.PoolArgs}
+               "specdec_pool_args": sd.PoolArgs, "specdec_keep_bound": sd.KeepBound}
     fields = "\n".join(f"F({cn}, {f})" for cn, py in structs.items() for f, _ in py._fields_)
     src = tmp_path / "probe.c"
     src.write_text(STRUCT_PROBE.replace("%FIELDS%", fields))

@@ -24,7 +24,8 @@ TOL_DRAW = 1e-5
 TOL_RESID = 1e-5
 
 
-def gpu_sample(tl, dl, draft, u, T, row_stride=None, residual=True):
+def gpu_sample(tl, dl, draft, u, T, row_stride=None, residual=True, top_k=0, top_p=1.0,
+               bounds_out=None):
     import speculative_decoding_specdec_gb300.specdec as sd
     B, Dp1, V = tl.shape
 
@@ -40,7 +41,14 @@ def gpu_sample(tl, dl, draft, u, T, row_stride=None, residual=True):
     y = torch.full((B,), -5, dtype=torch.int32, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     res = torch.full((B, V), -1.0, device=DEV) if residual else None
-    sd.verify_sample(place(tl), place(dl), draft.to(DEV), u.to(DEV), T, a, y, st, res)
+    tl_d, dl_d = place(tl), place(dl)
+    bounds = None
+    if top_k or top_p < 1.0:
+        bounds = torch.zeros((B, 2 * Dp1 - 1, 2), dtype=torch.int32, device=DEV)
+        sd.sampling_filter(tl_d, dl_d, T, top_k, top_p, bounds, st)
+        if bounds_out is not None:
+            bounds_out.append(bounds)
+    sd.verify_sample(tl_d, dl_d, draft.to(DEV), u.to(DEV), T, a, y, st, res, keep_bounds=bounds)
     torch.cuda.synchronize()
     return (a.cpu().numpy(), y.cpu().numpy(), None if res is None else res.cpu().numpy(),
             int(st.item()))
@@ -159,3 +167,165 @@ def test_repeated_calls_deterministic():
     r1 = gpu_sample(tl, dl, draft, u, 0.7, residual=False)
     r2 = gpu_sample(tl, dl, draft, u, 0.7, residual=False)
     assert (r1[0] == r2[0]).all() and (r1[1] == r2[1]).all()
+
+
+# ------------------------------------------------------------------ top-k / top-p
+
+def kept_from_bounds(scores, bound):
+    """Host decoding of one specdec_keep_bound: the order-preserving key of the float score
+    (-0 as +0; sign bit set for x >= 0, all bits inverted for x < 0) against (key, index)."""
+    x = np.asarray(scores, dtype=np.float32).copy()
+    x[x == 0] = 0.0
+    u = x.view(np.uint32)
+    key = np.where(u & 0x80000000, ~u, u | 0x80000000).astype(np.uint32)
+    bkey, bidx = np.uint32(bound[0] & 0xffffffff), int(bound[1])
+    return (key > bkey) | ((key == bkey) & (np.arange(len(x)) <= bidx))
+
+
+def rows_of(tl, dl):
+    """The 2D+1 score rows of every batch row, in the bounds' order (target rows, then draft)."""
+    return np.concatenate([tl, dl], axis=1)
+
+
+@pytest.mark.parametrize("B,D,V,dtype,top_k,top_p", [
+    (4, 3, 1000, torch.float32, 10, 1.0),
+    (4, 3, 1000, torch.float32, 0, 0.9),
+    (5, 3, 1003, torch.bfloat16, 37, 0.8),
+    (8, 5, 32000, torch.bfloat16, 50, 1.0),
+    (8, 5, 32000, torch.bfloat16, 0, 0.95),
+    (32, 6, 151552, torch.bfloat16, 0, 0.9),        # GLM-4-9B-shaped, top-p only
+    (32, 6, 151552, torch.bfloat16, 100, 0.95),     # top-k then top-p
+])
+def test_keep_bounds_match_the_oracle(B, D, V, dtype, top_k, top_p):
+    """Every row's kept set from the GPU bounds equals the oracle's (top-k exactly; top-p except
+    where top_p lies within 2e-6 of a cumulative mass, which fixed-point sums may cut either way)."""
+    import speculative_decoding_specdec_gb300.specdec as sd
+    gen = synth.make_gen(3000 + B + D + top_k)
+    tl, dl, draft, u = synth.sampled_round(gen, B, D, V, 0.7, dtype=dtype)
+    bounds = torch.zeros((B, 2 * D + 1, 2), dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sd.sampling_filter(tl.to(DEV), dl.to(DEV), 0.7, top_k, top_p, bounds, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    bnd = bounds.cpu().numpy().astype(np.int64)
+    rows = rows_of(tl.float().numpy(), dl.float().numpy())
+    excused = 0
+    for b in range(B):
+        for q in range(2 * D + 1):
+            got = kept_from_bounds(rows[b, q], bnd[b, q])
+            exp = O.sampling_keep(rows[b, q].astype(np.float64), 0.7, top_k, top_p)
+            if not np.array_equal(got, exp):
+                assert O.top_p_margin(rows[b, q].astype(np.float64), 0.7, top_k, top_p) < 2e-6, (b, q)
+                excused += 1
+    assert excused <= max(1, 0.02 * B * (2 * D + 1))
+
+
+def filtered_drafts(dl, T, top_k, top_p, seed):
+    """Drafts drawn from the oracle's filtered draft distribution q' of every draft row (so that
+    q'(d) > 0, as a draft model using the same sampling settings would propose)."""
+    rng = np.random.default_rng(seed)
+    w = dl.double().numpy()
+    B, D, V = w.shape
+    out = np.zeros((B, D), dtype=np.int32)
+    for b in range(B):
+        for j in range(D):
+            out[b, j] = rng.choice(V, p=O.filtered_softmax(w[b, j], T, top_k, top_p))
+    return torch.tensor(out)
+
+
+def compare_filtered(tl, dl, draft, u, T, top_k, top_p, max_excused=0.05):
+    a, y, res, st = gpu_sample(tl, dl, draft, u, T, top_k=top_k, top_p=top_p)
+    assert st == 0
+    tl64, dl64 = tl.double().numpy(), dl.double().numpy()
+    ea, ey, eres, tr = O.verify_sample(tl64, dl64, draft.numpy(), u.double().numpy(), T,
+                                       top_k=top_k, top_p=top_p)
+    rows = rows_of(tl64, dl64)
+    uu = u.double().numpy()
+    excused = 0
+    for b in range(len(a)):
+        close_cut = min(O.top_p_margin(r, T, top_k, top_p) for r in rows[b]) < 2e-6
+        if a[b] != ea[b]:
+            j = min(a[b], ea[b])
+            assert close_cut or abs(uu[b, j] - tr["ratio"][b, j]) < TOL_ACCEPT, (b, j)
+            excused += 1
+            continue
+        if y[b] != ey[b]:
+            near = min(abs(tr["t"][b] - tr["cdf_lo"][b]), abs(tr["t"][b] - tr["cdf_hi"][b]))
+            assert close_cut or near < TOL_DRAW * tr["R"][b], b
+            excused += 1
+            continue
+        if not close_cut:
+            np.testing.assert_allclose(res[b], eres[b], rtol=0, atol=TOL_RESID)
+    assert excused <= max(1, max_excused * len(a))
+    return a, y
+
+
+@pytest.mark.parametrize("B,D,V,T,dtype,top_k,top_p", [
+    (4, 4, 1000, 1.0, torch.float32, 20, 1.0),
+    (5, 3, 1003, 0.5, torch.bfloat16, 0, 0.9),      # ragged V: the cluster kernel's tail path
+    (8, 5, 32000, 0.7, torch.bfloat16, 64, 0.95),
+    (32, 6, 151552, 0.7, torch.bfloat16, 0, 0.9),   # GLM-4-9B-shaped
+    (16, 4, 151936, 0.7, torch.bfloat16, 200, 1.0), # Qwen3-8B-shaped: two CTAs per SM
+])
+def test_filtered_sample_matches_oracle(B, D, V, T, dtype, top_k, top_p):
+    gen = synth.make_gen(4000 + B + D)
+    tl, dl, _, u = synth.sampled_round(gen, B, D, V, T, dtype=dtype)
+    draft = filtered_drafts(dl, T, top_k, top_p, seed=B + D)
+    compare_filtered(tl, dl, draft, u, T, top_k, top_p)
+
+
+def test_filtered_padded_rows():
+    gen = synth.make_gen(41)
+    for dtype in (torch.bfloat16, torch.float32):
+        tl, dl, _, u = synth.sampled_round(gen, 6, 3, 5000, 0.7, dtype=dtype)
+        draft = filtered_drafts(dl, 0.7, 30, 1.0, seed=6)
+        a, y, res, st = gpu_sample(tl, dl, draft, u, 0.7, row_stride=5000 + 3, top_k=30)
+        ea, ey, _, _ = O.verify_sample(tl.double().numpy(), dl.double().numpy(), draft.numpy(),
+                                       u.double().numpy(), 0.7, top_k=30)
+        assert st == 0 and (a == ea).mean() >= 0.8
+
+
+def test_top_k_one_is_greedy_on_the_gpu():
+    """top_k = 1 with drafts equal to the draft rows' argmax gives the greedy verifier's result."""
+    gen = synth.make_gen(42)
+    B, D, V = 16, 5, 32000
+    tl, dl, _, u = synth.sampled_round(gen, B, D, V, 0.7, dtype=torch.bfloat16)
+    draft = dl.float().argmax(-1).to(torch.int32)
+    a, y, _, st = gpu_sample(tl, dl, draft, u, 0.7, residual=False, top_k=1)
+    ga, gy = O.verify_greedy(tl.double().numpy(), draft.numpy())
+    assert st == 0
+    np.testing.assert_array_equal(a, ga)
+    np.testing.assert_array_equal(y, gy)
+
+
+def test_filtered_emitted_token_follows_filtered_p():
+    rng = np.random.default_rng(43)
+    V, n, T = 8, 200000, 0.7
+    for k, tp in ((5, 1.0), (0, 0.8)):
+        zp0, zp1, zq = (rng.normal(size=V) for _ in range(3))
+        p0 = O.filtered_softmax(zp0, T, k, tp)
+        p1 = O.filtered_softmax(zp1, T, k, tp)
+        q0 = O.filtered_softmax(zq, T, k, tp)
+        tl = torch.tensor(np.stack([zp0, zp1]), dtype=torch.float32)[None].expand(n, 2, V).contiguous()
+        dl = torch.tensor(zq[None], dtype=torch.float32)[None].expand(n, 1, V).contiguous()
+        draft = torch.tensor(rng.choice(V, size=(n, 1), p=q0), dtype=torch.int32)
+        u = torch.tensor(rng.random((n, 2)), dtype=torch.float32)
+        a, y, _, st = gpu_sample(tl, dl, draft, u, T, residual=False, top_k=k, top_p=tp)
+        assert st == 0
+        first = np.where(a >= 1, draft[:, 0].numpy(), y)
+        m0, m1 = p0 > 0, p1 > 0
+        assert (np.bincount(first, minlength=V)[~m0] == 0).all()
+        assert stats.chisquare(np.bincount(first, minlength=V)[m0], p0[m0] * n).pvalue > 1e-3
+        bonus = y[a == 1]
+        assert stats.chisquare(np.bincount(bonus, minlength=V)[m1], p1[m1] * len(bonus)).pvalue > 1e-3
+
+
+def test_filter_host_errors():
+    import speculative_decoding_specdec_gb300.specdec as sd
+    gen = synth.make_gen(44)
+    tl, dl, draft, u = synth.sampled_round(gen, 2, 2, 100, 0.7, dtype=torch.float32)
+    bounds = torch.zeros((2, 5, 2), dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for k, p in ((0, 0.0), (0, 1.5), (-1, 1.0)):
+        with pytest.raises(sd.SpecdecError):
+            sd.sampling_filter(tl.to(DEV), dl.to(DEV), 0.7, k, p, bounds, st)
