@@ -38,6 +38,10 @@ def parse():
     p.add_argument("--workload", default="vicuna7b")
     p.add_argument("--impl", default="specdec", choices=["specdec", "reference"])
     p.add_argument("--copy-engine", type=int, default=0)
+    p.add_argument("--top-k", type=int, default=0,
+                   help="sampled workloads: top-k sampling setting (0: off)")
+    p.add_argument("--top-p", type=float, default=1.0,
+                   help="sampled workloads: top-p sampling setting (1: off)")
     p.add_argument("--ping-pong", action="store_true",
                    help="two K/V caches, realigned from one into the other (default: one cache "
                         "realigned in place)")
@@ -298,7 +302,8 @@ def run_specdec(args, rank, ws, local):
         if w.mode == "greedy":
             eng.verify_greedy(lg, d)
         else:
-            eng.verify_sample(lg, draft_logits[r], d, uniforms[r], w.temperature)
+            eng.verify_sample(lg, draft_logits[r], d, uniforms[r], w.temperature,
+                              top_k=args.top_k, top_p=args.top_p)
 
     # ---------------- device-resident timing
     eng.start(prompts)
@@ -341,6 +346,7 @@ def run_specdec(args, rank, ws, local):
         moved_cols += int(cols.sum())
     realign_bytes = 2.0 * moved_cols * w.token_bytes / K
     es = torch.tensor([], dtype=w.logit_dtype).element_size()
+    filtered = w.mode == "sampled" and (args.top_k or args.top_p < 1.0)  # + the filter kernel
     verify_bytes = (w.B * (w.D + 1) * w.V * es + (w.B * w.D * w.V * es if w.mode == "sampled" else 0)
                     + w.B * w.D * 4 + w.B * 8)
     committed = float(sum(int(a.sum()) + len(a) for a in acc)) / K
@@ -367,7 +373,8 @@ def run_specdec(args, rank, ws, local):
             else:
                 dev_dl.copy_(pin_dl[r], non_blocking=True)
                 dev_u.copy_(pin_u[r], non_blocking=True)
-                eng.verify_sample(dev_lg, dev_dl, dev_d, dev_u, w.temperature)
+                eng.verify_sample(dev_lg, dev_dl, dev_d, dev_u, w.temperature,
+                                  top_k=args.top_k, top_p=args.top_p)
             eng.realign(dev_d, copy_engine=args.copy_engine)
             if i is not None:
                 out[i, :w.B].copy_(eng.accept_len, non_blocking=True)
@@ -409,11 +416,13 @@ def run_specdec(args, rank, ws, local):
                      "frac": round(achieved / peak, 4),
                      "traffic": captured_traffic("realign_kernel", realign_bytes),
                      "bytes_per_launch": realign_bytes, "ms_per_launch": t_realign},
-        "verify": {"kernel": "greedy_kernel" if w.mode == "greedy" else "sample_kernel",
+        "verify": {"kernel": "greedy_kernel" if w.mode == "greedy" else
+                   ("filter_kernel + sample_kernel" if filtered else "sample_kernel"),
                    "ms_per_launch": t_verify, "bytes_per_launch": verify_bytes,
                    "achieved_gbs": round(verify_gbs, 1), "frac": round(verify_gbs / peak, 4),
-                   "traffic": captured_traffic("greedy_kernel" if w.mode == "greedy"
-                                               else "sample_kernel", verify_bytes)},
+                   "traffic": None if filtered else
+                   captured_traffic("greedy_kernel" if w.mode == "greedy" else "sample_kernel",
+                                    verify_bytes)},
         "committed_slots_per_s": committed / (ms_max / K / 1e3),
         "committed_per_round": committed,
         "cap_cols": cap,
@@ -639,10 +648,12 @@ def main():
     args = parse()
     rank, ws, local = dist_setup(args.gpus)
     w = workload(args)
+    filtered = w.mode == "sampled" and (args.top_k > 0 or args.top_p < 1.0)  # + the filter kernel
     config = {"workload": f"{w.name}: L={w.layers} KV heads={w.heads} head_dim={w.head_dim} "
                           f"B={w.B} D={w.D} V={w.V} {w.mode} verify",
               "B": w.B, "D": w.D, "V": w.V, "layers": w.layers, "kv_heads": w.heads,
               "head_dim": w.head_dim, "verify": w.mode,
+              **({"top_k": args.top_k, "top_p": args.top_p} if filtered else {}),
               "l2": "inputs larger than L2: every round streams >= 1 GB of K/V; all rounds' "
                     "score rows are distinct and generated before the timed region",
               "parallelism": f"replicas x{ws}"}
@@ -690,7 +701,8 @@ def main():
         line.update(value=res["value"], ms_per_step=res["ms_per_step"], clocks=res["clocks"],
                     e2e=res["e2e"], roofline=res["roofline"], verify=res["verify"],
                     committed_token_slots_per_s=res["committed_slots_per_s"],
-                    committed_per_round=res["committed_per_round"], gpu_launches=2 * args.steps,
+                    committed_per_round=res["committed_per_round"],
+                    gpu_launches=(3 if filtered else 2) * args.steps,
                     cpu_baseline=cpu)
         line["config"]["cap_cols"] = res["cap_cols"]
         line["config"]["kv_buffers"] = 2 if args.ping_pong else 1

@@ -12,12 +12,14 @@
 // token with score x at index v is kept iff key(x) > bound.key, or key(x) == bound.key and
 // v <= bound.index, where key is the order-preserving 32-bit code of the score.
 //
-// GB300 mapping.  One CTA per row at a time (a grid of up to two CTAs per SM walks the rows).  The
+// GB300 mapping.  One CTA per row at a time (a grid of one CTA per SM walks the rows).  The
 // bound is found by radix selection over the order-preserving key of the score's own bits (16 for
-// bf16, 32 for fp32), 8 bits per level, highest first: a 256-bin histogram in shared memory per
-// level (counts for top-k, masses for top-p), one warp picks the bin where the running total from
-// the top reaches the target, and the next level looks only inside it.  Ties on the final key are
-// resolved by index with a block scan.  Masses are 2^(x*c2 - o) (c2 = log2(e)/T, o the row's
+// bf16 as 11 + 5 bits, 32 for fp32 as 11 + 11 + 10), highest level first: a histogram in shared
+// memory per level (counts for top-k, masses for top-p; 2048 bins at the first level, since score
+// keys crowd into few exponent bins and narrower histograms serialise their atomics); one warp
+// picks the bin where the running total from the top reaches the target, and the next level looks
+// only inside it.  Ties on the final key are
+// resolved by index from per-chunk counts.  Masses are 2^(x*c2 - o) (c2 = log2(e)/T, o the row's
 // integer offset) in 64-bit fixed point, so every sum is an exact integer sum and the result does
 // not depend on the order of the atomics.  The row is read once from HBM; the later passes hit L2.
 #include <algorithm>
@@ -47,15 +49,48 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 
 template <typename T> struct Bits;
 template <> struct Bits<uint16_t> {  // bf16
-  static constexpr int K = 16;
+  static constexpr int K = 16, VN = 8;
   __device__ static uint32_t raw(const uint16_t* p) { return *p; }
   __device__ static float value(uint32_t raw) { return __uint_as_float(raw << 16); }
+  __device__ static uint32_t lane(const uint4& v, int i) {  // element i of a 16-byte vector
+    const uint32_t w = (&v.x)[i >> 1];
+    return (i & 1) ? (w >> 16) : (w & 0xffffu);
+  }
 };
 template <> struct Bits<float> {
-  static constexpr int K = 32;
+  static constexpr int K = 32, VN = 4;
   __device__ static uint32_t raw(const float* p) { return __float_as_uint(*p); }
   __device__ static float value(uint32_t raw) { return __uint_as_float(raw); }
+  __device__ static uint32_t lane(const uint4& v, int i) { return (&v.x)[i]; }
 };
+
+// Calls fn(i, raw) for every element of a row of V scores, all threads of the CTA together:
+// 16-byte vectors, four in flight per thread, when the row is 16-byte aligned; then the tail.
+template <typename T, typename Fn>
+__device__ __forceinline__ void visit_row(const T* x, int V, bool vec, Fn fn) {
+  constexpr int VN = Bits<T>::VN;
+  int done = 0;
+  if (vec) {
+    const uint4* v4 = reinterpret_cast<const uint4*>(x);
+    const int nv = V / VN;
+    for (int base = threadIdx.x; base < nv; base += 4 * kFThreads) {
+      uint4 r[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (base + k * kFThreads < nv) r[k] = v4[base + k * kFThreads];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int u = base + k * kFThreads;
+        if (u < nv) {
+#pragma unroll
+          for (int i = 0; i < VN; ++i) fn(u * VN + i, Bits<T>::lane(r[k], i));
+        }
+      }
+    }
+    done = nv * VN;
+  }
+  for (int i = done + static_cast<int>(threadIdx.x); i < V; i += kFThreads) fn(i, Bits<T>::raw(x + i));
+}
 
 // Order-preserving code of the score's own K bits, and its inverse.
 template <typename T>
@@ -84,11 +119,16 @@ struct FilterArgs {
   int32_t* status;
 };
 
-struct Shared {
-  uint32_t cnt[256];
-  unsigned long long mass[256];
-  uint32_t wcnt[kFThreads / 32];
-  unsigned long long wmass[kFThreads / 32];
+constexpr int kWarpsF = kFThreads / 32;
+constexpr int kBins = 2048;  // widest radix level: 11 key bits
+constexpr int kParts = 4;    // a mass (<= 2^44) as 11-bit parts, each summed in 32 bits
+
+struct Shared {  // dynamic shared memory
+  uint32_t cnt[kBins];
+  uint32_t part[kParts][kBins];
+  uint32_t steps[4096];                         // matches per step of the tie search
+  uint32_t wcnt[kWarpsF];
+  unsigned long long wmass[kWarpsF];
   uint32_t r_u[4];
   unsigned long long r_m[2];
 };
@@ -101,7 +141,7 @@ __device__ uint32_t block_max(uint32_t v, Shared& s) {
   if (lane == 0) s.wcnt[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    uint32_t x = lane < kFThreads / 32 ? s.wcnt[lane] : 0u;
+    uint32_t x = lane < kWarpsF ? s.wcnt[lane] : 0u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(0xffffffffu, x, o));
     if (lane == 0) s.r_u[0] = x;
@@ -112,49 +152,47 @@ __device__ uint32_t block_max(uint32_t v, Shared& s) {
   return r;
 }
 
-// Warp 0 picks, from the 256 bins of this level (bin 255 first), the bin where the running total
-// from the top first reaches `target` (1 <= target <= total); writes the bin and the total of the
-// bins above it.  `use_mass` selects the mass histogram, else the counts.
-__device__ void pick_bin(Shared& s, bool use_mass, unsigned long long target) {
+// Warp 0 walks `nb` totals in the given direction (from entry nb-1 down, or from 0 up) and finds
+// the entry where the running total first reaches `target` (1 <= target <= total); writes the
+// entry to r_u[1] and the total before it to r_m[0].  `vals(e)` gives entry e's total.
+template <typename Vals>
+__device__ void pick(Shared& s, int nb, bool top_down, unsigned long long target, Vals vals) {
   if (threadIdx.x >= 32) return;
   const int lane = threadIdx.x;
-  unsigned long long v[8], tot = 0;  // lane l holds bins 255-8l .. 248-8l, top first
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int b = 255 - 8 * lane - i;
-    v[i] = use_mass ? s.mass[b] : s.cnt[b];
-    tot += v[i];
-  }
+  const int per = (nb + 31) / 32;  // entries per lane, lane 0 first in walking order
+  auto entry = [&](int k) { return top_down ? nb - 1 - k : k; };
+  auto val = [&](int k) -> unsigned long long { return k < nb ? vals(entry(k)) : 0ull; };
+  unsigned long long tot = 0;
+  for (int k = lane * per; k < (lane + 1) * per; ++k) tot += val(k);
   unsigned long long incl = tot;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += t;
   }
-  const unsigned long long above = incl - tot;  // bins of the lanes before this one
-  const bool here = above < target && target <= incl;
-  const unsigned mine = __ballot_sync(0xffffffffu, here);
+  const unsigned long long above = incl - tot;
+  const unsigned mine = __ballot_sync(0xffffffffu, above < target && target <= incl);
   const int owner = mine ? __ffs(static_cast<int>(mine)) - 1 : 31;
   if (lane == owner) {
     unsigned long long run = above;
-    int bin = 255 - 8 * lane - 7;
-    for (int i = 0; i < 8; ++i) {
-      if (run + v[i] >= target || i == 7) {
-        bin = 255 - 8 * lane - i;
-        break;
-      }
-      run += v[i];
+    int k = lane * per;
+    const int last = max(k, min(nb, (lane + 1) * per) - 1);
+    for (; k < last; ++k) {
+      const unsigned long long v = val(k);
+      if (run + v >= target) break;
+      run += v;
     }
-    s.r_u[1] = static_cast<uint32_t>(bin);
-    s.r_m[0] = run;  // total of the bins above the chosen one
+    s.r_u[1] = static_cast<uint32_t>(entry(k));
+    s.r_m[0] = run;
   }
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kFThreads) filter_kernel(const FilterArgs A) {
-  __shared__ Shared s;
-  constexpr int KB = Bits<T>::K, LV = KB / 8;
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(kFThreads, 1) filter_kernel(const FilterArgs A) {
+  extern __shared__ __align__(16) char smem_raw[];
+  Shared& s = *reinterpret_cast<Shared*>(smem_raw);
+  constexpr int KB = Bits<T>::K, VN = Bits<T>::VN;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Q = 2 * A.D + 1, V = A.V;
   const long long rows = static_cast<long long>(A.B) * Q;
   const bool use_k = A.top_k >= 1 && A.top_k < V;
@@ -169,90 +207,154 @@ __global__ void __launch_bounds__(kFThreads) filter_kernel(const FilterArgs A) {
       if (tid == 0) A.bounds[row] = bound;
       continue;
     }
+    const bool vec = (reinterpret_cast<uintptr_t>(x) % 16) == 0;
     // Highest score: the offset of the masses; a NaN or +inf row keeps everything (verification
     // reports such rows as invalid).
     uint32_t km = 0;
-    for (int i = tid; i < V; i += kFThreads) km = max(km, nkey<T>(Bits<T>::raw(x + i)));
+    visit_row(x, V, vec, [&](int, uint32_t raw) { km = max(km, nkey<T>(raw)); });
     km = block_max(km, s);
     const float vmax = Bits<T>::value(nraw<T>(km));
     const bool finite_max = vmax == vmax && vmax != INFINITY && vmax != -INFINITY;
-    const float o = finite_max ? ceilf(vmax * A.c2) : 0.f;
+    if (!finite_max) {
+      if (tid == 0) A.bounds[row] = bound;
+      continue;
+    }
+    const float o = ceilf(vmax * A.c2);
     auto weight = [&](uint32_t raw) -> unsigned long long {
       const float w = ex2(fmaf(Bits<T>::value(raw), A.c2, -o));
       return __float2ull_rz(w * kFixedScale);
     };
 
-    // Top-k: the k-th token of the order, by counts.  K-set = key > kkey or (== kkey and v <= kidx).
     uint32_t kkey = 0;
     int kidx = INT_MAX;
     auto in_k = [&](uint32_t key, int v) { return key > kkey || (key == kkey && v <= kidx); };
-    // Radix selection over the keys of the tokens that pass `pred`, by counts (mass = false) or
-    // masses; returns the final key and, through `rest`, the target left for its ties.
-    auto select = [&](bool mass, unsigned long long target, auto pred, unsigned long long& rest) {
+    auto all = [](uint32_t, int) { return true; };
+
+    // Radix selection over the keys passing `pred`, by counts or masses, from the top: bf16 keys
+    // in levels of 11 and 5 bits, fp32 keys 11 + 11 + 10.  Counts and the four 11-bit parts of
+    // the masses go to the shared histogram with 32-bit atomics (integer sums: the result does
+    // not depend on their order).  With `p_of_total` the target is that fraction of the first
+    // level's total (top-p).  Returns the final key; `rest` receives the target left for the ties
+    // on that key.
+    auto select = [&](bool mass, unsigned long long target, float p_of_total, auto pred,
+                      unsigned long long& rest) {
       uint32_t pre = 0;
-      for (int L = LV - 1; L >= 0; --L) {
-        for (int i = tid; i < 256; i += kFThreads) {
+      int done = 0;  // key bits fixed so far
+      for (int l = 0; l < (KB == 16 ? 2 : 3); ++l) {
+        const int bits = KB == 16 ? (l == 0 ? 11 : 5) : (l == 2 ? 10 : 11);
+        const int nb = 1 << bits, sh = KB - done - bits;
+        for (int i = tid; i < nb; i += kFThreads) {
           s.cnt[i] = 0u;
-          s.mass[i] = 0ull;
+#pragma unroll
+          for (int k = 0; k < kParts; ++k) s.part[k][i] = 0u;
         }
         __syncthreads();
-        const int sh = 8 * L;
-        for (int i = tid; i < V; i += kFThreads) {
-          const uint32_t raw = Bits<T>::raw(x + i);
+        visit_row(x, V, vec, [&](int i, uint32_t raw) {
           const uint32_t key = nkey<T>(raw);
-          if ((L == LV - 1 || (key >> (sh + 8)) == pre) && pred(key, i)) {
-            const int bin = (key >> sh) & 255;
-            if (mass) atomicAdd(&s.mass[bin], weight(raw));
-            else atomicAdd(&s.cnt[bin], 1u);
+          if ((done == 0 || (key >> (sh + bits)) == pre) && pred(key, i)) {
+            const int bin = static_cast<int>((key >> sh) & static_cast<uint32_t>(nb - 1));
+            if (mass) {
+              const unsigned long long w = weight(raw);
+#pragma unroll
+              for (int k = 0; k < kParts; ++k) {
+                // the top part also holds bit 44 (a mass of exactly 1): at most 2^11 per token
+                const uint32_t pk = static_cast<uint32_t>(k == kParts - 1 ? (w >> (11 * k)) : ((w >> (11 * k)) & 0x7ffull));
+                if (pk) atomicAdd(&s.part[k][bin], pk);
+              }
+            } else {
+              atomicAdd(&s.cnt[bin], 1u);
+            }
           }
+        });
+        __syncthreads();
+        auto bin_mass = [&](int e) -> unsigned long long {
+          unsigned long long m = 0;
+#pragma unroll
+          for (int k = 0; k < kParts; ++k) m += static_cast<unsigned long long>(s.part[k][e]) << (11 * k);
+          return m;
+        };
+        if (l == 0 && p_of_total < 1.f) {  // top-p: keep while mass before < ceil(p * total)
+          unsigned long long t = 0;
+          for (int i = tid; i < nb; i += kFThreads) t += bin_mass(i);
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o2);
+          if (lane == 0) s.wmass[warp] = t;
+          __syncthreads();
+          if (tid == 0) {
+            unsigned long long tt = 0;
+            for (int w = 0; w < kWarpsF; ++w) tt += s.wmass[w];
+            const unsigned long long tg =
+                static_cast<unsigned long long>(ceil(static_cast<double>(p_of_total) * static_cast<double>(tt)));
+            s.r_m[1] = tg == 0 ? 1 : tg;
+          }
+          __syncthreads();
+          target = s.r_m[1];
         }
+        pick(s, nb, true, target, [&](int e) -> unsigned long long {
+          return mass ? bin_mass(e) : static_cast<unsigned long long>(s.cnt[e]);
+        });
         __syncthreads();
-        pick_bin(s, mass, target);
-        __syncthreads();
-        pre = (pre << 8) | s.r_u[1];
+        pre = (pre << bits) | s.r_u[1];
         target -= s.r_m[0];
+        done += bits;
         __syncthreads();
       }
       rest = target;
       return pre;
     };
-    // The need-th (1-based) token in index order among those with key == tkey passing `pred`.
+    // The need-th (1-based) token in index order among those with key == tkey passing `pred`:
+    // every warp counts the matches of whole steps of 32*VN consecutive elements (16-byte loads),
+    // a prefix over the steps picks one, and warp 0 finds the token inside it.
     auto nth_index = [&](uint32_t tkey, unsigned long long need, auto pred) {
-      const int chunk = (V + kFThreads - 1) / kFThreads;
-      const int c0 = min(V, tid * chunk), c1 = min(V, c0 + chunk);
-      uint32_t c = 0;
-      for (int i = c0; i < c1; ++i) {
-        const uint32_t key = nkey<T>(Bits<T>::raw(x + i));
-        if (key == tkey && pred(key, i)) ++c;
-      }
-      const int lane = tid & 31, warp = tid >> 5;
-      uint32_t incl = c;
+      const int step = 32 * VN;
+      const int nst = (V + step - 1) / step;
+      auto count_lane = [&](int st, uint32_t* raws) {
+        const int e0 = st * step + lane * VN;
+        if (vec && e0 + VN <= V) {
+          const uint4 r = *reinterpret_cast<const uint4*>(x + e0);
 #pragma unroll
-      for (int o2 = 1; o2 < 32; o2 <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o2);
-        if (lane >= o2) incl += t;
+          for (int i = 0; i < VN; ++i) raws[i] = Bits<T>::lane(r, i);
+        } else {
+#pragma unroll
+          for (int i = 0; i < VN; ++i) raws[i] = e0 + i < V ? Bits<T>::raw(x + e0 + i) : 0u;
+        }
+        unsigned n = 0;
+#pragma unroll
+        for (int i = 0; i < VN; ++i) {
+          const uint32_t key = nkey<T>(raws[i]);
+          if (e0 + i < V && key == tkey && pred(key, e0 + i)) ++n;
+        }
+        return n;
+      };
+      if (tid == 0) s.r_u[2] = static_cast<uint32_t>(V - 1);  // (never used: need <= matches)
+      for (int st = warp; st < nst; st += kWarpsF) {
+        uint32_t raws[VN];
+        const unsigned n = __reduce_add_sync(0xffffffffu, count_lane(st, raws));
+        if (lane == 0) s.steps[st] = n;
       }
-      if (lane == 31) s.wcnt[warp] = incl;
+      __syncthreads();
+      pick(s, nst, false, need, [&](int e) -> unsigned long long { return s.steps[e]; });
       __syncthreads();
       if (warp == 0) {
-        const uint32_t wv = lane < kFThreads / 32 ? s.wcnt[lane] : 0u;
-        uint32_t xx = wv;
+        const int st = static_cast<int>(s.r_u[1]);
+        uint32_t raws[VN];
+        const unsigned n = count_lane(st, raws);
+        unsigned incl = n;
 #pragma unroll
         for (int o2 = 1; o2 < 32; o2 <<= 1) {
-          const uint32_t t = __shfl_up_sync(0xffffffffu, xx, o2);
-          if (lane >= o2) xx += t;
+          const unsigned t = __shfl_up_sync(0xffffffffu, incl, o2);
+          if (lane >= o2) incl += t;
         }
-        if (lane < kFThreads / 32) s.wcnt[lane] = xx - wv;
-      }
-      __syncthreads();
-      const unsigned long long before = (incl - c) + s.wcnt[warp];
-      if (before < need && need <= before + c) {
-        unsigned long long run = before;
-        for (int i = c0; i < c1; ++i) {
-          const uint32_t key = nkey<T>(Bits<T>::raw(x + i));
-          if (key == tkey && pred(key, i) && ++run == need) {
-            s.r_u[2] = static_cast<uint32_t>(i);
-            break;
+        const unsigned long long before = s.r_m[0] + (incl - n);
+        if (n > 0 && before < need && need <= before + n) {
+          unsigned long long r = before;
+          const int e0 = st * step + lane * VN;
+          for (int i = 0; i < VN; ++i) {
+            const uint32_t key = nkey<T>(raws[i]);
+            if (e0 + i < V && key == tkey && pred(key, e0 + i) && ++r == need) {
+              s.r_u[2] = static_cast<uint32_t>(e0 + i);
+              break;
+            }
           }
         }
       }
@@ -261,47 +363,20 @@ __global__ void __launch_bounds__(kFThreads) filter_kernel(const FilterArgs A) {
       __syncthreads();
       return idx;
     };
-    auto all = [](uint32_t, int) { return true; };
 
-    if (!finite_max) {
-      if (tid == 0) A.bounds[row] = bound;
-      continue;
-    }
     if (use_k) {
       unsigned long long rest = 0;
-      const uint32_t key = select(false, static_cast<unsigned long long>(A.top_k), all, rest);
+      const uint32_t key = select(false, static_cast<unsigned long long>(A.top_k), 1.f, all, rest);
       kidx = nth_index(key, rest, all);
       kkey = key;
     }
     uint32_t fkey = kkey;
     int fidx = kidx;
     if (use_p) {
-      // Mass of the top-k set (or of the row), then the token where the mass before it stops
-      // being below top_p of that total.
-      unsigned long long mk = 0;
-      for (int i = tid; i < V; i += kFThreads) {
-        const uint32_t raw = Bits<T>::raw(x + i);
-        if (in_k(nkey<T>(raw), i)) mk += weight(raw);
-      }
-      const int lane = tid & 31, warp = tid >> 5;
-#pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) mk += __shfl_xor_sync(0xffffffffu, mk, o2);
-      if (lane == 0) s.wmass[warp] = mk;
-      __syncthreads();
-      if (tid == 0) {
-        unsigned long long t = 0;
-        for (int w = 0; w < kFThreads / 32; ++w) t += s.wmass[w];
-        // Keep a token iff (mass before it) < top_p * total, i.e. (mass before) < ceil(...).
-        const double tau = static_cast<double>(A.top_p) * static_cast<double>(t);
-        unsigned long long target = static_cast<unsigned long long>(ceil(tau));
-        if (target == 0) target = 1;
-        s.r_m[1] = target;
-      }
-      __syncthreads();
-      const unsigned long long target = s.r_m[1];
-      __syncthreads();
+      // The token where the mass before it (within the top-k set, or the row) stops being below
+      // top_p of that set's total.
       unsigned long long rest = 0;
-      const uint32_t key = select(true, target, in_k, rest);
+      const uint32_t key = select(true, 1ull, A.top_p, in_k, rest);
       // Inside the final key every kept token weighs the same w: the m-th one (index order) is
       // the last kept, m = ceil(rest / w).
       const unsigned long long w = weight(nraw<T>(key));
@@ -350,11 +425,24 @@ extern "C" int specdec_sampling_filter(const void* target_logits, const void* dr
   A.bounds = static_cast<uint2*>(keep_bounds);
   A.status = dev_status;
   const long long rows = static_cast<long long>(B) * (2 * D + 1);
-  const int grid = static_cast<int>(std::min<long long>(rows, 2LL * sms));
+  const int grid = static_cast<int>(std::min<long long>(rows, sms));
+  const int smem = static_cast<int>(sizeof(Shared));
+  static bool attr_set[2][64] = {{false}};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPECDEC_ERR_CUDA;
+  const int which = dtype == SPECDEC_BF16 ? 0 : 1;
+  if (!attr_set[which][dev]) {
+    const cudaError_t e = which == 0
+        ? cudaFuncSetAttribute(filter_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+        : cudaFuncSetAttribute(filter_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return map_cuda_error(e);
+    attr_set[which][dev] = true;
+  }
+  if (V > 4096 * 32 * (16 / es)) return SPECDEC_ERR_UNSUPPORTED;  // steps of the tie search
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dtype == SPECDEC_BF16)
-    filter_kernel<uint16_t><<<grid, kFThreads, 0, s>>>(A);
+  if (which == 0)
+    filter_kernel<uint16_t><<<grid, kFThreads, smem, s>>>(A);
   else
-    filter_kernel<float><<<grid, kFThreads, 0, s>>>(A);
+    filter_kernel<float><<<grid, kFThreads, smem, s>>>(A);
   return map_cuda_error(cudaGetLastError());
 }
