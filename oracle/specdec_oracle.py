@@ -53,6 +53,20 @@ Readings where the pages leave a step open (each is listed again in the design doc):
 * Length grouping: within one length, rows in index order fill whole batches of ``bs`` first; the
   remaining rows of every length, in (length, index) order, are chunked into mixed batches.
   Uniform batches come first (ascending length), then mixed batches.
+* Length-window grouping (window w >= 0): walk the rows in (length, index) order; where the next
+  ``bs`` rows span at most w in length they form a windowed batch, otherwise the row becomes a
+  leftover.  w = 0 is the exact-length rule above.  Windowed batches come first, then the
+  leftovers in (length, index) order cut into mixed batches.  Only a windowed batch of one length
+  is flagged uniform (verified in place).
+* SequencePool lifecycle: a slot is FREE, ACTIVE, or FINISHED (by end-of-sequence token or by its
+  length limit).  Only ACTIVE slots are grouped ("a pool of active sequences").  A sequence
+  finishes at the first newly committed position q with token == eos_id or q + 1 == its length
+  limit (the end-of-sequence token wins at the same position); its length becomes q + 1 and the
+  later tokens of that round are dropped.  A schedule reports each FINISHED slot once and frees
+  it.  Admission puts a prompt (N >= 1 tokens, N < limit) into a FREE slot with arena range
+  [col, col + cap), where limit + D - 1 <= cap and limit + D <= ids_cap, so that every round of
+  an unfinished sequence has room.  Arena ranges are given first fit: the lowest column where
+  enough consecutive columns are free.
 """
 from __future__ import annotations
 
@@ -73,6 +87,12 @@ __all__ = [
     "group_by_length",
     "pool_gather",
     "pool_append",
+    "FREE", "ACTIVE", "FINISHED_EOS", "FINISHED_LENGTH",
+    "group_by_window",
+    "pool_schedule",
+    "retire",
+    "pool_admit",
+    "FirstFitArena",
 ]
 
 
@@ -459,3 +479,160 @@ def pool_append(arena, slot_cols, slot_len, rows, scratch, width: int, accept_le
             ids_out[s, nb:nb + a] = np.asarray(draft[i, :a])
             ids_out[s, nb + a] = int(out_token[i])
     return out, new_len, ids_out
+
+
+# --------------------------------------------------------------------------------------------
+# SequencePool lifecycle  [BSDDR 2.3: "a pool of active sequences" grouped by length; only the
+# mixed-length ones are realigned]
+# --------------------------------------------------------------------------------------------
+
+FREE, ACTIVE, FINISHED_EOS, FINISHED_LENGTH = 0, 1, 2, 3
+
+
+def group_by_window(lengths, batch_size: int, window: int):
+    """Group rows into batches by a length window.
+
+    Walk the rows in (length, index) order.  At row position i, if the ``batch_size`` rows
+    i .. i + batch_size - 1 span at most ``window`` in length, they form a windowed batch and the
+    walk moves past them; otherwise row i is a leftover and the walk moves on by one.  The
+    leftovers, in (length, index) order, are cut into mixed batches of at most ``batch_size``.
+    With window 0 this is the exact-length rule of ``group_by_length``.
+    Returns (perm[N], batch_offsets[nb+1], batch_uniform[nb], num_windowed); a windowed batch is
+    flagged uniform iff all its rows have one length, a mixed batch never.
+    """
+    lengths = [int(x) for x in lengths]
+    if batch_size < 1 or window < 0:
+        raise OracleError("batch size / window")
+    order = sorted(range(len(lengths)), key=lambda i: (lengths[i], i))
+    sl = [lengths[i] for i in order]
+    n = len(order)
+    batches, uniform, leftover = [], [], []
+    i = 0
+    while i < n:
+        last = i + batch_size - 1
+        if last < n and sl[last] - sl[i] <= window:
+            batches.append(order[i:last + 1])
+            uniform.append(1 if sl[last] == sl[i] else 0)
+            i = last + 1
+        else:
+            leftover.append(order[i])
+            i += 1
+    num_windowed = len(batches)
+    for k in range(0, len(leftover), batch_size):
+        batches.append(leftover[k:k + batch_size])
+        uniform.append(0)
+    perm = np.array([r for bt in batches for r in bt], dtype=np.int32)
+    offsets = np.zeros(len(batches) + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum([len(bt) for bt in batches])
+    return perm, offsets, np.array(uniform, dtype=np.uint8), num_windowed
+
+
+def pool_schedule(state, slot_len, batch_size: int, window: int = 0):
+    """One scheduling step of the pool.
+
+    The ACTIVE slots (in slot order) are grouped by ``group_by_window``; perm lists slots.  Every
+    FINISHED slot is reported once, in slot order, with its state as the reason, and becomes FREE.
+    Returns a dict with perm, offsets, uniform, num_windowed, num_active, finished, reason and
+    the new state.
+    """
+    state = np.asarray(state, dtype=np.uint8)
+    slot_len = np.asarray(slot_len)
+    if (state > FINISHED_LENGTH).any():
+        raise OracleError("slot state")
+    active = [s for s in range(len(state)) if state[s] == ACTIVE]
+    if any(int(slot_len[s]) < 1 for s in active):
+        raise OracleError("empty sequence")
+    perm, offsets, uniform, nw = group_by_window([int(slot_len[s]) for s in active], batch_size,
+                                                 window)
+    finished = [s for s in range(len(state)) if state[s] in (FINISHED_EOS, FINISHED_LENGTH)]
+    new_state = state.copy()
+    new_state[finished] = FREE
+    return {"perm": np.array([active[i] for i in perm], dtype=np.int32), "offsets": offsets,
+            "uniform": uniform, "num_windowed": nw, "num_active": len(active),
+            "finished": np.array(finished, dtype=np.int32),
+            "reason": state[finished].astype(np.uint8), "state": new_state}
+
+
+def retire(len_before, len_after, pool_ids, rows, slot_limit, eos_id: int, state):
+    """Retirement after an append: for each slot s in ``rows``, scan the tokens committed this
+    round, positions q = len_before[s] .. len_after[s] - 1 in order.  At the first q whose token
+    is ``eos_id`` the sequence finishes by end of sequence; else at the first q with q + 1 ==
+    slot_limit[s] it finishes by length.  Either way its length becomes q + 1.
+    Returns (slot_len_out, state_out)."""
+    new_len = np.array(len_after, copy=True)
+    new_state = np.array(state, dtype=np.uint8, copy=True)
+    for s in rows:
+        for q in range(int(len_before[s]), int(len_after[s])):
+            if int(pool_ids[s][q]) == eos_id:
+                new_len[s], new_state[s] = q + 1, FINISHED_EOS
+                break
+            if q + 1 >= int(slot_limit[s]):
+                new_len[s], new_state[s] = q + 1, FINISHED_LENGTH
+                break
+    return new_len, new_state
+
+
+def pool_admit(state, slot_col, slot_cap, slot_len, slot_limit, pool_ids, slots, cols, caps,
+               limits, prompts, D: int, arena_cols: int):
+    """Admit prompts into FREE slots: slot s = slots[i] gets arena columns [cols[i], cols[i] +
+    caps[i]), limit limits[i], length len(prompts[i]) and the prompt as its first tokens; it
+    becomes ACTIVE.  Nothing changes if any entry is invalid: a slot out of range, not FREE or
+    named twice, an empty prompt, a prompt not shorter than its limit, or a range outside the
+    arena (OracleError "range"); limit + D - 1 > cap or limit + D > ids_cap (OracleError
+    "capacity").  Returns the new (state, slot_col, slot_cap, slot_len, slot_limit, pool_ids)."""
+    S, ids_cap = np.asarray(pool_ids).shape
+    if len(set(int(x) for x in slots)) != len(slots):
+        raise OracleError("range")
+    for i, s in enumerate(slots):
+        s, n, lim, c0, cap = int(s), len(prompts[i]), int(limits[i]), int(cols[i]), int(caps[i])
+        if not (0 <= s < S) or state[s] != FREE or n < 1 or n >= lim or c0 < 0 or cap < 1 \
+                or c0 + cap > arena_cols:
+            raise OracleError("range")
+        if lim + D - 1 > cap or lim + D > ids_cap:
+            raise OracleError("capacity")
+    out = [np.array(x, copy=True) for x in (state, slot_col, slot_cap, slot_len, slot_limit,
+                                            pool_ids)]
+    st, col, cap, ln, lim, ids = out
+    for i, s in enumerate(slots):
+        s = int(s)
+        st[s], col[s], cap[s] = ACTIVE, int(cols[i]), int(caps[i])
+        ln[s], lim[s] = len(prompts[i]), int(limits[i])
+        ids[s, :len(prompts[i])] = np.asarray(prompts[i])
+    return st, col, cap, ln, lim, ids
+
+
+class FirstFitArena:
+    """Arena columns [0, cols) handed out first fit: an allocation of n columns takes the lowest
+    column c with [c, c + n) all free.  Kept as a plain occupancy bitmap."""
+
+    def __init__(self, cols: int):
+        if cols < 1:
+            raise OracleError("arena size")
+        self.used = np.zeros(cols, dtype=bool)
+        self.blocks = {}
+
+    def alloc(self, n: int) -> int:
+        if n < 1:
+            raise OracleError("size")
+        cols = len(self.used)
+        for c in range(cols - n + 1):
+            if not self.used[c:c + n].any():
+                self.used[c:c + n] = True
+                self.blocks[c] = n
+                return c
+        raise OracleError("capacity")
+
+    def free(self, c: int) -> None:
+        if c not in self.blocks:
+            raise OracleError("not an allocation")
+        self.used[c:c + self.blocks.pop(c)] = False
+
+    def free_cols(self) -> int:
+        return int((~self.used).sum())
+
+    def largest_free(self) -> int:
+        best = run = 0
+        for u in self.used:
+            run = 0 if u else run + 1
+            best = max(best, run)
+        return best
