@@ -11,7 +11,9 @@
  *      and position-ID contiguity hold again.
  * For a pool of sequences, specdec_group_by_length forms batches of equal-length rows (which
  * need no realignment) and batches of mixed leftovers, and specdec_pool_gather /
- * specdec_pool_append move a mixed batch between the pool and a padded batch buffer.
+ * specdec_pool_append move a mixed batch between the pool and a padded batch buffer.  The pool's
+ * lifecycle (specdec_pool_admit, retirement inside specdec_pool_append, specdec_pool_schedule,
+ * and the host allocator of arena columns specdec_arena_*) lets sequences join and leave it.
  *
  * Sources (page title, section):
  *   [IE5]   "Inference Engineering: Part 5/8: When Speculative Decoding Backfires"
@@ -21,7 +23,8 @@
  *
  * Conventions for every entry point:
  *   - All array arguments are DEVICE pointers owned by the caller.  The library allocates no
- *     memory and keeps no state between calls.  Greedy verification also takes a caller-owned
+ *     device memory and keeps no state between calls (the host arena allocator objects, which
+ *     the caller creates and destroys, are the one exception).  Greedy verification also takes a caller-owned
  *     device WORKSPACE (size from specdec_verify_greedy_workspace, 256-byte aligned) through which
  *     its CTAs exchange per-row results.  Zero-fill it once before its first use: every call
  *     leaves it all zero again (also when it reports an out-of-range input through dev_status),
@@ -349,10 +352,118 @@ typedef struct {
   const int32_t* draft;         /* [n_rows][D] (or [S][D] with by_slot) append only */
   int by_slot;                  /* append: index the three arrays above by slot */
   int32_t* dev_status;          /* [1] */
+  /* Retirement (append only; slot_state NULL: none).  See "SequencePool lifecycle" below. */
+  uint8_t* slot_state;          /* [S] specdec_slot_state of each slot */
+  const int32_t* slot_limit;    /* [S] length limit of each slot */
+  int32_t eos_id;               /* end-of-sequence token id (< 0: length limit only) */
 } specdec_pool_args;
 
 int specdec_pool_gather(const specdec_pool_args* args, void* stream);
 int specdec_pool_append(const specdec_pool_args* args, void* stream);
+
+/*
+ * SequencePool lifecycle.  [BSDDR section 2.3: the pool holds the *active* sequences; those of one
+ * length are batched without realignment and only mixed-length ones are realigned.]
+ *
+ * Each slot s has a state byte slot_state[s]:
+ *     FREE --specdec_pool_admit--> ACTIVE --retirement in specdec_pool_append--> FINISHED_*
+ *     FINISHED_* --specdec_pool_schedule (reported once)--> FREE
+ * Only ACTIVE slots are scheduled.  A finished slot keeps its tokens (pool_ids[s][0 .. slot_len[s]))
+ * and K/V until it is admitted again.
+ *
+ * Retirement (specdec_pool_append with slot_state != NULL and slot_limit != NULL): after the
+ *   append of batch row i (slot s, old length N = batch_len[i], new length N + a_i + 1), the
+ *   committed positions q = N .. N + a_i are scanned in order; at the first q whose token is
+ *   eos_id the slot becomes FINISHED_EOS, else at the first q with q + 1 == slot_limit[s] it
+ *   becomes FINISHED_LENGTH; either way slot_len[s] = q + 1 (later tokens of the round are
+ *   dropped).  A row whose slot is not ACTIVE sets SPECDEC_ERR_INPUT_RANGE and its length, ids
+ *   and state are left alone (its K/V columns past N - 1 may still be written: name ACTIVE slots).
+ *
+ * specdec_pool_schedule: groups the ACTIVE slots by length window and lists the finished ones.
+ *   Rule: walk the ACTIVE slots in (slot_len, slot) order; where the next batch_size of them span
+ *   at most `window` in length they form a windowed batch and the walk moves past them, else the
+ *   slot is a leftover and the walk moves on by one.  Windowed batches come first, then the
+ *   leftovers, in (length, slot) order, cut into mixed batches of batch_size (the last may be
+ *   shorter).  window = 0 is the exact-length rule of specdec_group_by_length (over the ACTIVE
+ *   slots).  batch_uniform[k] = 1 only for a windowed batch of one length.
+ *   Outputs: perm[0 .. num_active) slots in batch order; batch k is perm[batch_offsets[k] ..
+ *   batch_offsets[k+1]); finished[0 .. num_finished) the FINISHED slots in slot order with their
+ *   state in finished_reason, and those slots are set FREE; counts = {num_batches, num_windowed,
+ *   num_active, num_finished}.  Entries past the counts are not written.
+ *   Limits: 0 <= S <= 4096, 1 <= batch_size <= 4096, window >= 0; ACTIVE lengths in [1, 2^20).
+ *   A state above FINISHED_LENGTH or an ACTIVE length out of range sets SPECDEC_ERR_INPUT_RANGE
+ *   and nothing is written.  One CTA; latency-bound.
+ */
+typedef enum {
+  SPECDEC_SLOT_FREE = 0,
+  SPECDEC_SLOT_ACTIVE = 1,
+  SPECDEC_SLOT_FINISHED_EOS = 2,
+  SPECDEC_SLOT_FINISHED_LENGTH = 3
+} specdec_slot_state;
+
+typedef struct {
+  int S, batch_size, window;
+  uint8_t* slot_state;          /* [S] read; FINISHED slots set FREE */
+  const int32_t* slot_len;      /* [S] */
+  int32_t* perm;                /* [S] out */
+  int32_t* batch_offsets;       /* [S+1] out */
+  uint8_t* batch_uniform;       /* [S] out */
+  int32_t* finished;            /* [S] out */
+  uint8_t* finished_reason;     /* [S] out */
+  int32_t* counts;              /* [4] out */
+  int32_t* dev_status;          /* [1] */
+} specdec_schedule_args;
+
+int specdec_pool_schedule(const specdec_schedule_args* args, void* stream);
+
+/*
+ * specdec_pool_admit: put n prompts into FREE slots.  Entry i: slot slots[i] gets arena columns
+ *   [cols[i], cols[i] + caps[i]), length limit limits[i], slot_len = its prompt length, pool_ids
+ *   row = the prompt (prompt_ids[prompt_off[i] .. prompt_off[i+1])), and becomes ACTIVE.  The
+ *   prompt's K/V is the caller's (the target's prefill writes it).
+ *   Every entry is checked first: slot in [0, S), FREE and named once; prompt length >= 1 and
+ *   below its limit; arena range inside [0, arena_cols) (else SPECDEC_ERR_INPUT_RANGE);
+ *   limit + D - 1 <= caps[i] and limit + D <= ids_cap, so that every round until the limit has
+ *   room (else SPECDEC_ERR_CAPACITY).  On any error nothing is written.  The writes are also
+ *   skipped when dev_status is nonzero on entry.  Arena ranges of different slots must not
+ *   overlap (not checked: the arena allocator below hands out disjoint runs); the prompt buffer
+ *   must hold prompt_off[n] tokens.
+ *   Limits: 0 <= n <= 1024, 0 <= S <= 4096, 1 <= D <= 31.  Two launches (check, then write).
+ */
+typedef struct {
+  int n, S, D, ids_cap;
+  int64_t arena_cols;
+  const int32_t* slots;         /* [n] */
+  const int32_t* cols;          /* [n] first arena column */
+  const int32_t* caps;          /* [n] arena columns */
+  const int32_t* limits;        /* [n] length limit */
+  const int32_t* prompt_ids;    /* [prompt_off[n]] */
+  const int32_t* prompt_off;    /* [n+1] */
+  uint8_t* slot_state;          /* [S] */
+  int32_t* slot_col;            /* [S] */
+  int32_t* slot_cap;            /* [S] */
+  int32_t* slot_len;            /* [S] */
+  int32_t* slot_limit;          /* [S] */
+  int32_t* pool_ids;            /* [S][ids_cap] */
+  int32_t* dev_status;          /* [1] */
+} specdec_admit_args;
+
+int specdec_pool_admit(const specdec_admit_args* args, void* stream);
+
+/*
+ * Arena allocator (HOST only, thread safe).  Columns [0, cols) of the pool's K/V arena are handed
+ * out first fit: specdec_arena_alloc returns the lowest column c with [c, c + ncols) free
+ * (SPECDEC_ERR_CAPACITY if there is none); specdec_arena_free takes the start of an allocation
+ * (SPECDEC_ERR_INVALID_ARG otherwise) and merges the run with free neighbours.  The arena object
+ * is created and destroyed by the caller; no GPU is touched.
+ */
+typedef struct specdec_arena specdec_arena;
+int specdec_arena_create(int64_t cols, specdec_arena** out);
+void specdec_arena_destroy(specdec_arena* arena);
+int specdec_arena_alloc(specdec_arena* arena, int64_t ncols, int64_t* col);
+int specdec_arena_free(specdec_arena* arena, int64_t col);
+int specdec_arena_stats(specdec_arena* arena, int64_t* free_cols, int64_t* largest_free,
+                        int64_t* allocations);
 
 #ifdef __cplusplus
 }

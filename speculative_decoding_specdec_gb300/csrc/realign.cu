@@ -88,6 +88,9 @@ struct Params {
   uint8_t* s_mask;
   int32_t* s_pos;
   int scratch_cap, arena_cap;
+  uint8_t* slot_state;  // append: retirement when set
+  const int32_t* slot_limit;
+  int32_t eos_id;
   int32_t* status;
 };
 
@@ -410,10 +413,30 @@ __device__ void write_metadata(const Params& p, const Plan& s, long long gt, lon
       const int sl = p.rows[r];
       const int N = s.aux[r], a = s.acc[r];
       const int src = p.by_slot ? sl : r;  // row of accept_len / out_token / draft
+      if (p.slot_state && p.slot_state[sl] != SPECDEC_SLOT_ACTIVE) {
+        set_status(p.status, SPECDEC_ERR_INPUT_RANGE);
+        continue;
+      }
       int32_t* ids = p.pool_ids + static_cast<long long>(sl) * p.ids_cap;
       for (int q = 0; q < a; ++q) ids[N + q] = p.draft[static_cast<long long>(src) * p.D + q];
       ids[N + a] = p.out_token[src];
-      p.slot_len[sl] = N + a + 1;
+      int len = N + a + 1;
+      if (p.slot_state) {  // retirement: first end-of-sequence token or the length limit
+        const int lim = p.slot_limit[sl];
+        for (int q = N; q <= N + a; ++q) {
+          if (ids[q] == p.eos_id) {
+            len = q + 1;
+            p.slot_state[sl] = SPECDEC_SLOT_FINISHED_EOS;
+            break;
+          }
+          if (q + 1 >= lim) {
+            len = q + 1;
+            p.slot_state[sl] = SPECDEC_SLOT_FINISHED_LENGTH;
+            break;
+          }
+        }
+      }
+      p.slot_len[sl] = len;
     }
   }
 }
@@ -546,6 +569,7 @@ int pool_common(const specdec_pool_args* a, Params& p, bool append) {
   if (!append && !a->in_place && (!a->scratch_ids || !a->scratch_mask || !a->scratch_pos))
     return SPECDEC_ERR_INVALID_ARG;
   if (append && (!a->accept_len || !a->out_token || !a->draft)) return SPECDEC_ERR_INVALID_ARG;
+  if (append && a->slot_state && !a->slot_limit) return SPECDEC_ERR_INVALID_ARG;
   uintptr_t alo, ahi, slo, shi;
   view_span(ar, alo, ahi);
   view_span(sc, slo, shi);
@@ -579,6 +603,9 @@ int pool_common(const specdec_pool_args* a, Params& p, bool append) {
   p.s_pos = a->scratch_pos;
   p.scratch_cap = sc.cap_cols;
   p.arena_cap = ar.cap_cols;
+  p.slot_state = append ? a->slot_state : nullptr;
+  p.slot_limit = a->slot_limit;
+  p.eos_id = a->eos_id;
   p.status = a->dev_status;
   return SPECDEC_OK;
 }

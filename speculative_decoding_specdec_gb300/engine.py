@@ -235,3 +235,165 @@ class ExspecPool:
                             self.slot_len, self.pool_ids, self.batch_len[:n], self.width,
                             self.accept_len, self.out_token, draft, self.status,
                             in_place=uniform, by_slot=True, stream=stream)
+
+
+class SequencePool:
+    """EXSPEC SequencePool with its lifecycle (one GPU): sequences are admitted into free slots,
+    scheduled each round in batches by length window, verified, committed, and retired by the
+    end-of-sequence token or their length limit.
+
+    Device state: slot_state / slot_col / slot_cap / slot_len / slot_limit [S] and pool_ids
+    [S, ids_cap]; K/V in one arena [L, 2, 1, H, arena_cols, hd] whose column runs are handed out
+    by the host first-fit allocator (``specdec.Arena``).  The host keeps which slots are taken
+    (admitted and not yet reported finished) and which run each one holds; it learns of finished
+    sequences from the schedule's readback, the one device-to-host copy of a round, which also
+    decides the calls that follow.
+
+    A round: ``schedule()`` -> [admit()] -> verify (all slots, by slot) -> per batch
+    ``gather()`` / (the target's verification pass writes K/V) / ``append()``.  Uniform batches are
+    verified in place in their slots (no K/V is moved); windowed and mixed ones go through the
+    padded batch buffer.
+    """
+
+    def __init__(self, layers, heads, head_dim, kv_dtype, S, arena_cols, D, max_len,
+                 batch_size=8, window=0, eos_id=-1, device="cuda", pad_id=0):
+        dev = torch.device(device)
+        self.S, self.D, self.bs, self.window = S, D, batch_size, window
+        self.eos_id, self.pad_id, self.max_len = eos_id, pad_id, max_len
+        self.arena_cols = arena_cols
+        self.arena = torch.empty((layers, 2, 1, heads, arena_cols, head_dim), dtype=kv_dtype,
+                                 device=dev)
+        self.alloc = specdec.Arena(arena_cols)
+        i32 = dict(dtype=torch.int32, device=dev)
+        u8 = dict(dtype=torch.uint8, device=dev)
+        self.slot_state = torch.zeros(S, **u8)
+        self.slot_col = torch.zeros(S, **i32)
+        self.slot_cap = torch.zeros(S, **i32)
+        self.slot_len = torch.zeros(S, **i32)
+        self.slot_limit = torch.zeros(S, **i32)
+        self.ids_cap = max_len + D + 1
+        self.pool_ids = torch.full((S, self.ids_cap), pad_id, **i32)
+        sc_cap = max_len + D + 1
+        self.scratch = torch.empty((layers, 2, batch_size, heads, sc_cap, head_dim),
+                                   dtype=kv_dtype, device=dev)
+        self.scratch_ids = torch.zeros((batch_size, sc_cap), **i32)
+        self.scratch_mask = torch.zeros((batch_size, sc_cap), **u8)
+        self.scratch_pos = torch.zeros((batch_size, sc_cap), **i32)
+        self.batch_len = torch.zeros(batch_size, **i32)
+        self.width = torch.zeros(1, **i32)
+        self.perm = torch.zeros(S, **i32)
+        self.offsets = torch.zeros(S + 1, **i32)
+        self.uniform = torch.zeros(S, **u8)
+        self.finished = torch.zeros(S, **i32)
+        self.reason = torch.zeros(S, **u8)
+        self.counts = torch.zeros(4, **i32)
+        self.accept_len = torch.zeros(S, **i32)
+        self.out_token = torch.zeros(S, **i32)
+        self.status = torch.zeros(1, **i32)
+        self.workspaces = Workspaces(dev)
+        # schedule readback: counts | offsets | uniform | finished | reason (int32 each)
+        self._host = torch.zeros(4 + (S + 1) + 3 * S, dtype=torch.int32).pin_memory()
+        self._dev_rb = torch.zeros_like(self._host, device=dev)
+        self.taken = [False] * S          # admitted and not yet reported finished
+        self.run_of = [None] * S          # arena run of each taken slot
+
+    # -------------------------------------------------------------- admission
+    def admit(self, prompts, limits, stream=None):
+        """Admit as many of ``prompts`` (token lists, in order) as there are free slots and arena
+        room for; returns their slots (a prefix of the prompts is admitted).  Each needs
+        limit + D - 1 arena columns.  The prompt's K/V is the caller's to write (prefill) at
+        columns [slot_col, slot_col + len - 1) of the arena."""
+        slots, cols, caps = [], [], []
+        free = [s for s in range(self.S) if not self.taken[s]]
+        for p, lim in zip(prompts, limits):
+            if not free:
+                break
+            if lim > self.max_len or len(p) < 1 or len(p) >= lim:
+                raise ValueError("prompt length / limit out of range")
+            need = lim + self.D - 1
+            c = self.alloc.alloc(need)
+            if c is None:
+                break
+            s = free.pop(0)
+            slots.append(s)
+            cols.append(c)
+            caps.append(need)
+        n = len(slots)
+        if n == 0:
+            return []
+        lens = [len(p) for p in prompts[:n]]
+        off = [0]
+        for x in lens:
+            off.append(off[-1] + x)
+        flat = [t for p in prompts[:n] for t in p]
+        host = torch.tensor(slots + cols + caps + list(limits[:n]) + off + flat,
+                            dtype=torch.int32).pin_memory()
+        st = stream or torch.cuda.current_stream()
+        with torch.cuda.stream(st):       # one copy of every argument, then the two launches
+            dev = host.to(self.slot_len.device, non_blocking=True)
+            v = [dev[k * n:(k + 1) * n] for k in range(4)]
+            specdec.pool_admit(v[0], v[1], v[2], v[3], dev[5 * n + 1:], dev[4 * n:5 * n + 1],
+                               self.D, self.arena_cols, self.slot_state, self.slot_col,
+                               self.slot_cap, self.slot_len, self.slot_limit, self.pool_ids,
+                               self.status, st)
+        for s, c in zip(slots, cols):
+            self.taken[s] = True
+            self.run_of[s] = c
+        return slots
+
+    # -------------------------------------------------------------- schedule
+    def schedule(self, stream=None):
+        """Schedule the round on the device and read it back once.  Returns (batches, finished):
+        batches as (offset, rows, uniform) into ``perm``; finished as (slot, reason) -- those
+        slots' tokens stay readable (``tokens``) until they are admitted again, and their arena
+        runs are returned to the allocator now."""
+        specdec.pool_schedule(self.slot_state, self.slot_len, self.bs, self.window, self.perm,
+                              self.offsets, self.uniform, self.finished, self.reason, self.counts,
+                              self.status, stream)
+        S, rb = self.S, self._dev_rb
+        rb[0:4].copy_(self.counts, non_blocking=True)
+        rb[4:5 + S].copy_(self.offsets, non_blocking=True)
+        rb[5 + S:5 + 2 * S].copy_(self.uniform, non_blocking=True)
+        rb[5 + 2 * S:5 + 3 * S].copy_(self.finished, non_blocking=True)
+        rb[5 + 3 * S:5 + 4 * S].copy_(self.reason, non_blocking=True)
+        self._host.copy_(rb, non_blocking=True)
+        (stream or torch.cuda.current_stream()).synchronize()
+        h = self._host.tolist()
+        nb, nf = h[0], h[3]
+        off = h[4:5 + S]
+        uni = h[5 + S:5 + 2 * S]
+        fin = list(zip(h[5 + 2 * S:5 + 2 * S + nf], h[5 + 3 * S:5 + 3 * S + nf]))
+        for s, _ in fin:
+            self.alloc.free(self.run_of[s])
+            self.taken[s] = False
+            self.run_of[s] = None
+        return [(off[k], off[k + 1] - off[k], bool(uni[k])) for k in range(nb)], fin
+
+    def tokens(self, slot):
+        """Committed tokens of a slot (a device-to-host copy)."""
+        n = int(self.slot_len[slot].item())
+        return self.pool_ids[slot, :n].tolist()
+
+    # -------------------------------------------------------------- one round's calls
+    def verify_greedy(self, logits, draft, stream=None):
+        """Greedy verification of every slot: logits [S, D+1, V], draft [S, D] in slot order
+        (rows of slots that are not scheduled are ignored)."""
+        specdec.verify_greedy(logits, draft, self.accept_len, self.out_token, self.status,
+                              self.workspaces.greedy(logits, draft), stream)
+
+    def gather(self, off, n, uniform, stream=None):
+        """Repad batch perm[off:off+n] into the batch buffer (uniform batches: lengths only)."""
+        specdec.pool_gather(self.arena, self.scratch, self.perm[off:off + n], self.D,
+                            self.slot_col, self.slot_cap, self.slot_len, self.pool_ids,
+                            self.batch_len[:n], self.width, self.status, self.scratch_ids,
+                            self.scratch_mask, self.scratch_pos, pad_id=self.pad_id,
+                            in_place=uniform, stream=stream)
+
+    def append(self, off, n, uniform, draft, stream=None):
+        """Commit batch perm[off:off+n] back to its slots and retire finished sequences."""
+        specdec.pool_append(self.arena, self.scratch, self.perm[off:off + n], self.D,
+                            self.slot_col, self.slot_cap, self.slot_len, self.pool_ids,
+                            self.batch_len[:n], self.width, self.accept_len, self.out_token,
+                            draft, self.status, in_place=uniform, by_slot=True,
+                            slot_state=self.slot_state, slot_limit=self.slot_limit,
+                            eos_id=self.eos_id, stream=stream)

@@ -55,7 +55,32 @@ class PoolArgs(ctypes.Structure):
                 ("scratch_ids", ctypes.c_void_p), ("scratch_mask", ctypes.c_void_p),
                 ("scratch_pos", ctypes.c_void_p), ("accept_len", ctypes.c_void_p),
                 ("out_token", ctypes.c_void_p), ("draft", ctypes.c_void_p),
-                ("by_slot", ctypes.c_int), ("dev_status", ctypes.c_void_p)]
+                ("by_slot", ctypes.c_int), ("dev_status", ctypes.c_void_p),
+                ("slot_state", ctypes.c_void_p), ("slot_limit", ctypes.c_void_p),
+                ("eos_id", ctypes.c_int32)]
+
+
+class ScheduleArgs(ctypes.Structure):
+    _fields_ = [("S", ctypes.c_int), ("batch_size", ctypes.c_int), ("window", ctypes.c_int),
+                ("slot_state", ctypes.c_void_p), ("slot_len", ctypes.c_void_p),
+                ("perm", ctypes.c_void_p), ("batch_offsets", ctypes.c_void_p),
+                ("batch_uniform", ctypes.c_void_p), ("finished", ctypes.c_void_p),
+                ("finished_reason", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("dev_status", ctypes.c_void_p)]
+
+
+class AdmitArgs(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int), ("S", ctypes.c_int), ("D", ctypes.c_int),
+                ("ids_cap", ctypes.c_int), ("arena_cols", ctypes.c_int64),
+                ("slots", ctypes.c_void_p), ("cols", ctypes.c_void_p), ("caps", ctypes.c_void_p),
+                ("limits", ctypes.c_void_p), ("prompt_ids", ctypes.c_void_p),
+                ("prompt_off", ctypes.c_void_p), ("slot_state", ctypes.c_void_p),
+                ("slot_col", ctypes.c_void_p), ("slot_cap", ctypes.c_void_p),
+                ("slot_len", ctypes.c_void_p), ("slot_limit", ctypes.c_void_p),
+                ("pool_ids", ctypes.c_void_p), ("dev_status", ctypes.c_void_p)]
+
+
+SLOT_FREE, SLOT_ACTIVE, SLOT_FINISHED_EOS, SLOT_FINISHED_LENGTH = range(4)
 
 
 _vp, _ll, _i, _f = ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_float
@@ -86,6 +111,21 @@ if hasattr(lib, "specdec_verify_sample"):
                                           _vp, _vp, _vp, _vp]
 lib.specdec_sampling_filter.restype = _i
 lib.specdec_sampling_filter.argtypes = [_vp, _vp, _i, _i, _i, _i, _ll, _f, _i, _f, _vp, _vp, _vp]
+lib.specdec_pool_schedule.restype = _i
+lib.specdec_pool_schedule.argtypes = [ctypes.POINTER(ScheduleArgs), _vp]
+lib.specdec_pool_admit.restype = _i
+lib.specdec_pool_admit.argtypes = [ctypes.POINTER(AdmitArgs), _vp]
+_i64, _i64p = ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)
+lib.specdec_arena_create.restype = _i
+lib.specdec_arena_create.argtypes = [_i64, ctypes.POINTER(_vp)]
+lib.specdec_arena_destroy.restype = None
+lib.specdec_arena_destroy.argtypes = [_vp]
+lib.specdec_arena_alloc.restype = _i
+lib.specdec_arena_alloc.argtypes = [_vp, _i64, _i64p]
+lib.specdec_arena_free.restype = _i
+lib.specdec_arena_free.argtypes = [_vp, _i64]
+lib.specdec_arena_stats.restype = _i
+lib.specdec_arena_stats.argtypes = [_vp, _i64p, _i64p, _i64p]
 
 
 class KeepBound(ctypes.Structure):
@@ -337,13 +377,110 @@ def pool_gather(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids,
 
 
 def pool_append(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len, width,
-                accept_len, out_token, draft, status, in_place=False, by_slot=False, stream=None):
+                accept_len, out_token, draft, status, in_place=False, by_slot=False,
+                slot_state=None, slot_limit=None, eos_id=-1, stream=None):
     """Append a verified batch back to its pool slots (see specdec.h).  With ``by_slot`` the
-    accept lengths, tokens and drafts are pool-wide arrays indexed by slot."""
+    accept lengths, tokens and drafts are pool-wide arrays indexed by slot.  With ``slot_state``
+    (and ``slot_limit``) finished sequences are retired: end-of-sequence token ``eos_id`` or the
+    length limit."""
     a = _pool_args(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len,
                    width, status, 0, in_place)
     a.by_slot = int(bool(by_slot))
     for name, t in (("accept_len", accept_len), ("out_token", out_token), ("draft", draft)):
         _need(t, torch.int32, name)
         setattr(a, name, t.data_ptr())
+    if slot_state is not None:
+        _need(slot_state, torch.uint8, "slot_state")
+        _need(slot_limit, torch.int32, "slot_limit")
+        a.slot_state, a.slot_limit, a.eos_id = (slot_state.data_ptr(), slot_limit.data_ptr(),
+                                                int(eos_id))
     _check(lib.specdec_pool_append(ctypes.byref(a), _stream(stream)), "specdec_pool_append")
+
+
+# ------------------------------------------------------------------------ SequencePool lifecycle
+
+def pool_schedule(slot_state, slot_len, batch_size, window, perm, batch_offsets, batch_uniform,
+                  finished, finished_reason, counts, status, stream=None):
+    """Group the ACTIVE slots by length window, list (and free) the finished ones; counts =
+    {num_batches, num_windowed, num_active, num_finished} (see specdec.h)."""
+    S = slot_state.numel()
+    _need(slot_state, torch.uint8, "slot_state")
+    _need(batch_uniform, torch.uint8, "batch_uniform")
+    _need(finished_reason, torch.uint8, "finished_reason")
+    for t, n in ((slot_len, "slot_len"), (perm, "perm"), (batch_offsets, "batch_offsets"),
+                 (finished, "finished"), (counts, "counts"), (status, "status")):
+        _need(t, torch.int32, n)
+    if (slot_len.numel() < S or perm.numel() < S or batch_offsets.numel() < S + 1 or
+            batch_uniform.numel() < S or finished.numel() < S or finished_reason.numel() < S or
+            counts.numel() < 4):
+        raise ValueError("buffers too small")
+    a = ScheduleArgs()
+    a.S, a.batch_size, a.window = S, int(batch_size), int(window)
+    for name, t in (("slot_state", slot_state), ("slot_len", slot_len), ("perm", perm),
+                    ("batch_offsets", batch_offsets), ("batch_uniform", batch_uniform),
+                    ("finished", finished), ("finished_reason", finished_reason),
+                    ("counts", counts), ("dev_status", status)):
+        setattr(a, name, t.data_ptr())
+    _check(lib.specdec_pool_schedule(ctypes.byref(a), _stream(stream)), "specdec_pool_schedule")
+
+
+def pool_admit(slots, cols, caps, limits, prompt_ids, prompt_off, D, arena_cols, slot_state,
+               slot_col, slot_cap, slot_len, slot_limit, pool_ids, status, stream=None):
+    """Admit prompts (concatenated in ``prompt_ids``, bounds in ``prompt_off``) into FREE slots
+    (see specdec.h)."""
+    n = slots.numel()
+    _need(slot_state, torch.uint8, "slot_state")
+    for t, nm in ((slots, "slots"), (cols, "cols"), (caps, "caps"), (limits, "limits"),
+                  (prompt_ids, "prompt_ids"), (prompt_off, "prompt_off"), (slot_col, "slot_col"),
+                  (slot_cap, "slot_cap"), (slot_len, "slot_len"), (slot_limit, "slot_limit"),
+                  (pool_ids, "pool_ids"), (status, "status")):
+        _need(t, torch.int32, nm)
+    if cols.numel() < n or caps.numel() < n or limits.numel() < n or prompt_off.numel() < n + 1:
+        raise ValueError("per-entry arrays too small")
+    if pool_ids.dim() != 2 or not pool_ids.is_contiguous():
+        raise ValueError("pool_ids must be a contiguous [slots, ids_cap] int32 tensor")
+    a = AdmitArgs()
+    a.n, a.S, a.D, a.ids_cap = n, slot_state.numel(), int(D), pool_ids.shape[1]
+    a.arena_cols = int(arena_cols)
+    for name, t in (("slots", slots), ("cols", cols), ("caps", caps), ("limits", limits),
+                    ("prompt_ids", prompt_ids), ("prompt_off", prompt_off),
+                    ("slot_state", slot_state), ("slot_col", slot_col), ("slot_cap", slot_cap),
+                    ("slot_len", slot_len), ("slot_limit", slot_limit), ("pool_ids", pool_ids),
+                    ("dev_status", status)):
+        setattr(a, name, t.data_ptr())
+    _check(lib.specdec_pool_admit(ctypes.byref(a), _stream(stream)), "specdec_pool_admit")
+
+
+class Arena:
+    """Host first-fit allocator of arena columns (specdec_arena_*; no GPU involved)."""
+
+    def __init__(self, cols: int):
+        h = ctypes.c_void_p()
+        _check(lib.specdec_arena_create(int(cols), ctypes.byref(h)), "specdec_arena_create")
+        self._h = h
+        self.cols = int(cols)
+
+    def alloc(self, ncols: int):
+        """Lowest free run of ``ncols`` columns, or None when none is free."""
+        c = ctypes.c_int64()
+        rc = lib.specdec_arena_alloc(self._h, int(ncols), ctypes.byref(c))
+        if rc == ERR_CAPACITY:
+            return None
+        _check(rc, "specdec_arena_alloc")
+        return c.value
+
+    def free(self, col: int) -> None:
+        _check(lib.specdec_arena_free(self._h, int(col)), "specdec_arena_free")
+
+    def stats(self):
+        """(free columns, largest free run, allocations)."""
+        v = [ctypes.c_int64() for _ in range(3)]
+        _check(lib.specdec_arena_stats(self._h, *[ctypes.byref(x) for x in v]),
+               "specdec_arena_stats")
+        return tuple(x.value for x in v)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            lib.specdec_arena_destroy(h)
+            self._h = None

@@ -72,3 +72,29 @@ def eqspec_rounds(L, H, hd, kv_dtype, B, D, V, rounds, prompt_lo, prompt_hi, see
             toks[b] += draft[b, :a[b]].tolist() + [int(y[b])]
         history.append(a)
     return history
+
+
+# ------------------------------------------------------------------ SequencePool lifecycle runs
+
+D, V, EOS = 3, 24, 0   # draft length, vocabulary and end-of-sequence token of the lifecycle runs
+
+
+def round_scores(seq, r):
+    """The fp32 scores [D+1, V] and draft [D] of round r of sequence seq: the same whether the
+    sequence runs in a pool or alone."""
+    logits, draft = synth.greedy_round(synth.make_gen(7919 * seq + r), 1, D, V, 0.7,
+                                       dtype=torch.float32)
+    return logits[0], draft[0]
+
+
+def alone(prompt, limit, seq):
+    """The tokens a sequence commits when it runs by itself, and why it stops (oracle only)."""
+    toks, r = list(prompt), 0
+    while True:
+        logits, draft = round_scores(seq, r)
+        a, y = O.verify_greedy(logits.double().numpy()[None], draft.numpy()[None])
+        for t in draft[:a[0]].tolist() + [int(y[0])]:
+            toks.append(int(t))
+            if t == EOS or len(toks) >= limit:
+                return toks, (O.FINISHED_EOS if t == EOS else O.FINISHED_LENGTH)
+        r += 1

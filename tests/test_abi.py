@@ -13,7 +13,7 @@ HEADER = os.path.join(ROOT, "include", "specdec.h")
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\s*\*)\s+(specdec_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|void|const char\s*\*)\s+(specdec_\w+)\s*\(", text, re.M)))
 
 
 def test_every_declared_symbol_is_exported():
@@ -21,6 +21,7 @@ def test_every_declared_symbol_is_exported():
     names = declared_functions()
     assert "specdec_realign" in names and "specdec_verify_sample" in names
     assert "specdec_verify_greedy_workspace" in names and "specdec_verify_greedy_noalloc" in names
+    assert "specdec_pool_schedule" in names and "specdec_arena_destroy" in names
     missing = [n for n in names if not hasattr(sd.lib, n)]
     assert missing == []
     assert sd.version() == 100
@@ -51,6 +52,8 @@ int main(void) {
   printf("specdec_realign_args %zu\n", sizeof(specdec_realign_args));
   printf("specdec_pool_args %zu\n", sizeof(specdec_pool_args));
   printf("specdec_keep_bound %zu\n", sizeof(specdec_keep_bound));
+  printf("specdec_schedule_args %zu\n", sizeof(specdec_schedule_args));
+  printf("specdec_admit_args %zu\n", sizeof(specdec_admit_args));
   %FIELDS%
   return 0;
 }
@@ -60,7 +63,8 @@ int main(void) {
 def test_ctypes_layout_matches_c(tmp_path):
     import speculative_decoding_specdec_gb300.specdec as sd
     structs = {"specdec_kv_view": sd.KvView, "specdec_realign_args": sd.RealignArgs,
-               "specdec_pool_args": sd.PoolArgs, "specdec_keep_bound": sd.KeepBound}
+               "specdec_pool_args": sd.PoolArgs, "specdec_keep_bound": sd.KeepBound,
+               "specdec_schedule_args": sd.ScheduleArgs, "specdec_admit_args": sd.AdmitArgs}
     fields = "\n".join(f"F({cn}, {f})" for cn, py in structs.items() for f, _ in py._fields_)
     src = tmp_path / "probe.c"
     src.write_text(STRUCT_PROBE.replace("%FIELDS%", fields))
@@ -121,6 +125,65 @@ def test_host_validation_codes():
     assert L.specdec_pool_gather(None, None) == sd.ERR_INVALID_ARG
     p = sd.PoolArgs()
     assert L.specdec_pool_append(ctypes.byref(p), None) == sd.ERR_INVALID_ARG
+    # lifecycle: schedule and admission (host checks; no kernel runs)
+    assert L.specdec_pool_schedule(None, None) == sd.ERR_INVALID_ARG
+    g = sd.ScheduleArgs()
+    g.S, g.batch_size, g.window = 4, 0, 0
+    assert L.specdec_pool_schedule(ctypes.byref(g), None) == sd.ERR_INVALID_ARG   # batch size 0
+    g.batch_size, g.window = 8, -1
+    assert L.specdec_pool_schedule(ctypes.byref(g), None) == sd.ERR_INVALID_ARG   # negative window
+    g.S, g.window = 5000, 0
+    assert L.specdec_pool_schedule(ctypes.byref(g), None) == sd.ERR_UNSUPPORTED   # > 4096 slots
+    g.S = 4
+    assert L.specdec_pool_schedule(ctypes.byref(g), None) == sd.ERR_INVALID_ARG   # NULL buffers
+    m = sd.AdmitArgs()
+    m.n, m.S, m.D, m.ids_cap = 0, 4, 3, 16
+    assert L.specdec_pool_admit(ctypes.byref(m), None) == sd.OK                   # nothing to admit
+    m.n = 2
+    assert L.specdec_pool_admit(ctypes.byref(m), None) == sd.ERR_INVALID_ARG      # NULL buffers
+    m.n = 2000
+    assert L.specdec_pool_admit(ctypes.byref(m), None) == sd.ERR_UNSUPPORTED      # > 1024 entries
+    m.n, m.D = 2, 0
+    assert L.specdec_pool_admit(ctypes.byref(m), None) == sd.ERR_INVALID_ARG
+    assert L.specdec_pool_admit(None, None) == sd.ERR_INVALID_ARG
+    # retirement needs the limits
+    p.slot_state = 64
+    assert L.specdec_pool_append(ctypes.byref(p), None) == sd.ERR_INVALID_ARG
+
+
+def test_arena_allocator_matches_first_fit_oracle():
+    """The host allocator (C++) against the oracle's bitmap first fit: same columns for the same
+    sequence of requests and frees, same free totals."""
+    import numpy as np
+    import speculative_decoding_specdec_gb300.specdec as sd
+    import oracle.specdec_oracle as O
+    rng = np.random.default_rng(5)
+    for cols in (1, 17, 500):
+        a, o = sd.Arena(cols), O.FirstFitArena(cols)
+        live = []
+        for _ in range(400):
+            if live and rng.random() < 0.45:
+                c = live.pop(int(rng.integers(len(live))))
+                a.free(c)
+                o.free(c)
+            else:
+                n = int(rng.integers(1, max(2, cols // 4)))
+                got = a.alloc(n)
+                try:
+                    want = o.alloc(n)
+                except O.OracleError:
+                    want = None
+                assert got == want
+                if got is not None:
+                    live.append(got)
+            assert a.stats() == (o.free_cols(), o.largest_free(), len(live))
+        with pytest.raises(sd.SpecdecError):
+            a.free(cols + 5)                                       # not an allocation
+        with pytest.raises(sd.SpecdecError):
+            a.alloc(0)                                             # empty request
+        for c in live:
+            a.free(c)
+        assert a.stats() == (cols, cols, 0) and a.alloc(cols) == 0
 
 
 def test_binding_raises_on_host_error():

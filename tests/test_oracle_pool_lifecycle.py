@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import oracle.specdec_oracle as O
-from speculative_decoding_specdec_gb300 import synth
+import specdec_testlib as testlib
 
 
 # ------------------------------------------------------------------------- window grouping
@@ -193,27 +193,8 @@ def test_first_fit_sequence():
 
 # ------------------------------------------------------------------------- whole lifecycle
 
-D, V, EOS = 3, 24, 0
-
-
-def _round_scores(seq, r):
-    """The scores and draft of round r of sequence seq (the same whether pooled or alone)."""
-    import torch
-    logits, draft = synth.greedy_round(synth.make_gen(7919 * seq + r), 1, D, V, 0.7,
-                                       dtype=torch.float32)
-    return logits[0].double().numpy(), draft[0].numpy()
-
-
-def _alone(prompt, limit, seq):
-    toks, r = list(prompt), 0
-    while True:
-        logits, draft = _round_scores(seq, r)
-        a, y = O.verify_greedy(logits[None], draft[None])
-        for t in draft[:a[0]].tolist() + [int(y[0])]:
-            toks.append(int(t))
-            if t == EOS or len(toks) >= limit:
-                return toks, (O.FINISHED_EOS if t == EOS else O.FINISHED_LENGTH)
-        r += 1
+D, V, EOS = testlib.D, testlib.V, testlib.EOS
+_alone = testlib.alone
 
 
 def _pooled(requests, S, bs, window, arena_cols):
@@ -263,8 +244,8 @@ def _pooled(requests, S, bs, window, arena_cols):
         before = ln.copy()
         for k in range(len(off) - 1):
             rows = perm[off[k]:off[k + 1]].tolist()
-            logits = np.stack([_round_scores(seq_of[s], rnd[s])[0] for s in rows])
-            draft = np.stack([_round_scores(seq_of[s], rnd[s])[1] for s in rows])
+            logits = np.stack([testlib.round_scores(seq_of[s], rnd[s])[0] for s in rows])
+            draft = np.stack([testlib.round_scores(seq_of[s], rnd[s])[1] for s in rows])
             a, y = O.verify_greedy(logits, draft)
             if sch["uniform"][k]:
                 for i, s in enumerate(rows):               # verified in place in the slot
