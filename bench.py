@@ -42,6 +42,8 @@ def parse():
                    help="sampled workloads: top-k sampling setting (0: off)")
     p.add_argument("--top-p", type=float, default=1.0,
                    help="sampled workloads: top-p sampling setting (1: off)")
+    p.add_argument("--window", type=int, default=0,
+                   help="exspec_serving: length window of a batch (0: exact length)")
     p.add_argument("--ping-pong", action="store_true",
                    help="two K/V caches, realigned from one into the other (default: one cache "
                         "realigned in place)")
@@ -259,7 +261,8 @@ def measured_peaks():
 def workload(args):
     import dataclasses
     from speculative_decoding_specdec_gb300 import synth
-    w = synth.WORKLOADS["exspec_pool" if args.workload == "exspec_sweep" else args.workload]
+    w = synth.WORKLOADS["exspec_pool" if args.workload in ("exspec_sweep", "exspec_serving")
+                        else args.workload]
     return dataclasses.replace(w, layers=args.layers) if args.layers else w
 
 
@@ -289,7 +292,8 @@ def run_specdec(args, rank, ws, local):
             lg, d = synth.greedy_round(g, w.B, w.D, w.V, w.alpha, dtype=w.logit_dtype, device=dev)
         else:
             lg, dl, d, u = synth.sampled_round(g, w.B, w.D, w.V, w.temperature,
-                                               dtype=w.logit_dtype, device=dev)
+                                               dtype=w.logit_dtype, device=dev,
+                                               draft_candidates=args.top_k)
             draft_logits.append(dl)
             uniforms.append(u)
         logits.append(lg)
@@ -511,6 +515,142 @@ def run_pool(args, rank, ws):
             "mixed_rows_per_round": mixed_rows}
 
 
+# ------------------------------------------------------------------------------ serving pool
+
+def run_serving(args, rank, ws):
+    """The SequencePool lifecycle under a closed loop of requests on the pool workload's cache
+    (Vicuna-7B-shaped, 256 slots, D=5, V=32000): prompts from the 8 discrete lengths, each
+    generating U[32, 128] tokens (length limit) with end-of-sequence token 2.  A round is
+    schedule (+ one readback) -> admission of waiting requests into the freed slots and arena runs
+    -> greedy verification of every slot -> per batch gather / append with retirement.  The
+    prompts' K/V (the target's prefill) and the verification pass's K/V belong to the model and
+    are not written; the copies move the same bytes either way."""
+    import numpy as np
+    import torch
+    from speculative_decoding_specdec_gb300 import synth
+    from speculative_decoding_specdec_gb300.engine import SequencePool
+
+    w = workload(args)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    K, Wm = args.steps, args.warmup
+    R = K + Wm
+    S, D = w.B, w.D
+    gen = synth.make_gen(w.seed * 1000 + 17 + rank)
+    nreq = 6 * S
+    plen = synth.lengths_discrete(gen, nreq, w.prompt[1]).tolist()
+    limits = [int(n) + int(x) for n, x in zip(plen, torch.randint(32, 129, (nreq,), generator=gen))]
+    prompts = [torch.randint(0, w.V, (int(n),), generator=gen).tolist() for n in plen]
+    max_len = max(limits)
+    mean_need = float(np.mean(limits)) + D - 1
+    arena_cols = int(1.15 * mean_need * S)
+    free, _ = torch.cuda.mem_get_info()
+    need = (arena_cols + 8 * (max_len + D + 1)) * w.token_bytes + R * S * (D + 1) * w.V * 2
+    if need > 0.85 * free:
+        raise SystemExit(f"serving pool needs {need / 1e9:.0f} GB, {free / 1e9:.0f} GB free")
+    pool = SequencePool(w.layers, w.heads, w.head_dim, w.kv_dtype, S, arena_cols, D, max_len,
+                        batch_size=8, window=args.window, eos_id=2, device=dev)
+    alpha = (torch.rand(S, generator=gen) * 0.4 + 0.5).to(dev)    # acceptance U[0.5, 0.9] per slot
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    logits, drafts = [], []
+    for _ in range(R):
+        lg, d = synth.greedy_round(g, S, D, w.V, alpha, dtype=w.logit_dtype, device=dev)
+        logits.append(lg)
+        drafts.append(d)
+    nxt = 0
+
+    def admit():
+        nonlocal nxt
+        got = pool.admit(prompts[nxt:nxt + S], limits[nxt:nxt + S])
+        nxt += len(got)
+        return len(got)
+
+    pool.schedule()
+    admit()
+    stream = torch.cuda.current_stream()
+    stats = {"committed": 0, "finished": 0, "admitted": 0, "active": 0, "batches": 0,
+             "uniform_rows": 0, "rows": 0, "moved": 0, "pad": 0, "cols": 0}
+    dev_ms = []
+
+    def one_round(r, timed):
+        before = list(pool.host_len)
+        batches, fin = pool.schedule()
+        after = pool.host_len
+        prev = getattr(one_round, "prev_rows", [])
+        prev_mixed = getattr(one_round, "prev_mixed", [])
+        if timed:
+            stats["committed"] += sum(after[s] - before[s] for s in prev)
+            stats["finished"] += len(fin)
+            # append of the last round's gathered rows: a + 1 columns each (retirement may cut a
+            # sequence shorter, so this slightly undercounts)
+            stats["moved"] += 2 * sum(after[s] - before[s] for s in prev_mixed) * w.token_bytes
+        n_adm = admit()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(stream)
+        pool.verify_greedy(logits[r], drafts[r])
+        for off, k, uni in batches:
+            pool.gather(off, k, uni)
+            pool.append(off, k, uni, drafts[r])
+        ev[1].record(stream)
+        rows = pool.host_perm
+        mixed = [s for off, k, uni in batches if not uni for s in rows[off:off + k]]
+        one_round.prev_rows = rows
+        one_round.prev_mixed = mixed
+        if timed:
+            stats["moved"] += 2 * sum(after[s] - 1 for s in mixed) * w.token_bytes   # gather
+            for off, k, _ in batches:
+                lens = [after[s] for s in rows[off:off + k]]
+                stats["pad"] += sum(max(lens) - x for x in lens)
+                stats["cols"] += max(lens) * len(lens)
+            dev_ms.append(ev)
+            stats["admitted"] += n_adm
+            stats["active"] += len(rows)
+            stats["batches"] += len(batches)
+            stats["uniform_rows"] += sum(k for _, k, uni in batches if uni)
+            stats["rows"] += len(rows)
+
+    for r in range(Wm):
+        one_round(r, False)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for i in range(K):
+        one_round(Wm + i, True)
+    torch.cuda.synchronize()
+    wall = max_over_ranks(time.perf_counter() - t0, ws)
+    if int(pool.status.item()):
+        raise RuntimeError(f"device status {int(pool.status.item())}")
+    # the schedule kernel alone, on the final pool state (no finished slots left to report)
+    pool.schedule()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    from speculative_decoding_specdec_gb300 import specdec as sd
+    args_s = (pool.slot_state, pool.slot_len, pool.bs, pool.window, pool.perm, pool.offsets,
+              pool.uniform, pool.finished, pool.reason, pool.counts, pool.status)
+    for _ in range(5):
+        sd.pool_schedule(*args_s)
+    e0.record(stream)
+    for _ in range(50):
+        sd.pool_schedule(*args_s)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sched_us = e0.elapsed_time(e1) / 50 * 1e3
+    dev_total_s = sum(e[0].elapsed_time(e[1]) for e in dev_ms) / 1e3
+    peak, peak_kind = measured_peaks()
+    gbs = stats["moved"] / dev_total_s / 1e9
+    return {"value": sum_over_ranks(float(K), ws) / wall, "ms_per_step": wall / K * 1e3,
+            "device_ms_per_round": float(np.mean([e[0].elapsed_time(e[1]) for e in dev_ms])),
+            "committed_tokens_per_s": sum_over_ranks(float(stats["committed"]), ws) / wall,
+            "finished_per_round": stats["finished"] / K, "admitted_per_round": stats["admitted"] / K,
+            "active_rows_per_round": stats["active"] / K,
+            "batches_per_round": stats["batches"] / K,
+            "uniform_row_fraction": round(stats["uniform_rows"] / max(1, stats["rows"]), 3),
+            "pad_fraction": round(stats["pad"] / max(1, stats["cols"]), 4),
+            "moved_gb_per_round": round(stats["moved"] / K / 1e9, 2),
+            "gather_append_gbs": round(gbs, 1), "gather_append_frac": round(gbs / peak, 4),
+            "peak": peak, "peak_source": peak_kind,
+            "schedule_kernel_us": round(sched_us, 2), "slots": S, "arena_cols": arena_cols,
+            "window": args.window, "requests_admitted_total": nxt}
+
+
 # ------------------------------------------------------------------------------ batch sweep
 
 def run_sweep(args, rank, ws):
@@ -678,6 +818,18 @@ def main():
                                   f"batches of 8, greedy verify")
             line.update(value=res.pop("value"), ms_per_step=res.pop("ms_per_step"), pool=res,
                         unit="pool rounds/s", metric="EXSPEC pool rounds/s")
+            print(json.dumps(line))
+        return
+    if args.workload == "exspec_serving":
+        res = run_serving(args, rank, ws)
+        if rank == 0:
+            config["workload"] = (f"exspec_serving: {w.B} slots, L={w.layers} KV heads={w.heads} "
+                                  f"head_dim={w.head_dim}, D={w.D}, V={w.V}, prompts from "
+                                  f"{{256,...,2048}} generating U[32,128] tokens, acceptance "
+                                  f"U[0.5,0.9] per slot, batches of 8, window {args.window}, "
+                                  f"greedy verify")
+            line.update(value=res.pop("value"), ms_per_step=res.pop("ms_per_step"), pool=res,
+                        unit="rounds/s", metric="EXSPEC serving pool rounds/s")
             print(json.dumps(line))
         return
     if args.workload == "exspec_sweep":

@@ -12,16 +12,25 @@
 // token with score x at index v is kept iff key(x) > bound.key, or key(x) == bound.key and
 // v <= bound.index, where key is the order-preserving 32-bit code of the score.
 //
-// GB300 mapping.  One CTA per row at a time (a grid of one CTA per SM walks the rows).  The
-// bound is found by radix selection over the order-preserving key of the score's own bits (16 for
-// bf16 as 11 + 5 bits, 32 for fp32 as 11 + 11 + 10), highest level first: a histogram in shared
-// memory per level (counts for top-k, masses for top-p; 2048 bins at the first level, since score
-// keys crowd into few exponent bins and narrower histograms serialise their atomics); one warp
-// picks the bin where the running total from the top reaches the target, and the next level looks
-// only inside it.  Ties on the final key are
-// resolved by index from per-chunk counts.  Masses are 2^(x*c2 - o) (c2 = log2(e)/T, o the row's
-// integer offset) in 64-bit fixed point, so every sum is an exact integer sum and the result does
-// not depend on the order of the atomics.  The row is read once from HBM; the later passes hit L2.
+// GB300 mapping.  One CTA of 512 threads per row at a time (one CTA per SM walks the rows).
+//
+// bf16 rows: a bf16 score has only 65536 possible values, so one read of the row from HBM builds
+// a count per value in shared memory (16-bit counters, two to a 32-bit word, 128 KB; shared
+// atomics without return).  The highest score, the top-k cut (counts from the top) and the top-p
+// cut (count x per-value weight, from the top) then come from block scans over that histogram,
+// and one more pass (from L2) finds the index of the last kept token among the tokens of the cut
+// value.  If the counts do not add up to V (a counter passed 65535: more than 65535 equal scores)
+// the row takes the radix path instead.
+//
+// fp32 rows: radix selection over the order-preserving key of the score (11 + 11 + 10 bits),
+// highest level first: a shared-memory histogram per level (2048 bins at the first level, since
+// score keys crowd into few exponent values and narrower histograms serialise their atomics),
+// counts for top-k and masses for top-p; one warp picks the bin where the running total from the
+// top reaches the target, and the next level looks only inside it.  Ties on the final key are
+// resolved by index from per-step match counts.
+//
+// Masses are 2^(x*c2 - o) (c2 = log2(e)/T, o the row's integer offset) in 2^44 fixed point, so
+// every sum is an exact integer sum and no result depends on the order of the atomics.
 #include <algorithm>
 #include <climits>
 #include <cmath>
@@ -65,21 +74,21 @@ template <> struct Bits<float> {
 };
 
 // Calls fn(i, raw) for every element of a row of V scores, all threads of the CTA together:
-// 16-byte vectors, four in flight per thread, when the row is 16-byte aligned; then the tail.
-template <typename T, typename Fn>
+// 16-byte vectors, kFly in flight per thread, when the row is 16-byte aligned; then the tail.
+template <typename T, int kFly = 4, typename Fn>
 __device__ __forceinline__ void visit_row(const T* x, int V, bool vec, Fn fn) {
   constexpr int VN = Bits<T>::VN;
   int done = 0;
   if (vec) {
     const uint4* v4 = reinterpret_cast<const uint4*>(x);
     const int nv = V / VN;
-    for (int base = threadIdx.x; base < nv; base += 4 * kFThreads) {
-      uint4 r[4];
+    for (int base = threadIdx.x; base < nv; base += kFly * kFThreads) {
+      uint4 r[kFly];
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
+      for (int k = 0; k < kFly; ++k)
         if (base + k * kFThreads < nv) r[k] = v4[base + k * kFThreads];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kFly; ++k) {
         const int u = base + k * kFThreads;
         if (u < nv) {
 #pragma unroll
@@ -122,16 +131,24 @@ struct FilterArgs {
 constexpr int kWarpsF = kFThreads / 32;
 constexpr int kBins = 2048;  // widest radix level: 11 key bits
 constexpr int kParts = 4;    // a mass (<= 2^44) as 11-bit parts, each summed in 32 bits
+constexpr int kHistWords = 65536 / 2;  // bf16 value histogram: two 16-bit counters per word
 
 struct Shared {  // dynamic shared memory
   uint32_t cnt[kBins];
   uint32_t part[kParts][kBins];
   uint32_t steps[4096];                         // matches per step of the tie search
+  unsigned long long ctot[kFThreads];           // per-thread chunk totals of the bf16 histogram
   uint32_t wcnt[kWarpsF];
   unsigned long long wmass[kWarpsF];
+  int ovf;
   uint32_t r_u[4];
   unsigned long long r_m[2];
 };
+
+// The bf16 histogram follows Shared in dynamic shared memory, 128-byte aligned (it is cleared
+// with 16-byte stores).
+constexpr size_t kHistOffset = (sizeof(Shared) + 127) & ~static_cast<size_t>(127);
+static_assert(kHistOffset % 16 == 0, "histogram must be 16-byte aligned");
 
 // Block-wide max of one value per thread.
 __device__ uint32_t block_max(uint32_t v, Shared& s) {
@@ -187,11 +204,218 @@ __device__ void pick(Shared& s, int nb, bool top_down, unsigned long long target
   }
 }
 
+// The need-th (1-based) token in index order among those with key == tkey passing `pred`:
+// every warp counts the matches of whole steps of 32*VN consecutive elements (16-byte loads,
+// four steps in flight), a prefix over the steps picks one, and warp 0 finds the token in it.
+template <typename T, typename Pred>
+__device__ __forceinline__ int nth_index(const T* x, int V, bool vec, Shared& s, uint32_t tkey,
+                                         unsigned long long need, Pred pred) {
+  constexpr int VN = Bits<T>::VN;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int step = 32 * VN;
+  const int nst = (V + step - 1) / step;
+  // Matches among the lane's VN elements of step st (from its vector when the step is whole and
+  // the row aligned, else element by element).
+  auto count_lane = [&](int st, const uint4& r) {
+    const int e0 = st * step + lane * VN;
+    unsigned n = 0;
+    if (vec && e0 + VN <= V) {
+#pragma unroll
+      for (int i = 0; i < VN; ++i) {
+        const uint32_t key = nkey<T>(Bits<T>::lane(r, i));
+        n += (key == tkey && pred(key, e0 + i)) ? 1u : 0u;
+      }
+    } else {
+#pragma unroll 1
+      for (int i = 0; i < VN; ++i) {
+        if (e0 + i >= V) break;
+        const uint32_t key = nkey<T>(Bits<T>::raw(x + e0 + i));
+        n += (key == tkey && pred(key, e0 + i)) ? 1u : 0u;
+      }
+    }
+    return n;
+  };
+  auto load_lane = [&](int st) -> uint4 {
+    const int e0 = st * step + lane * VN;
+    if (vec && e0 + VN <= V) return *reinterpret_cast<const uint4*>(x + e0);
+    return make_uint4(0u, 0u, 0u, 0u);
+  };
+  if (tid == 0) s.r_u[2] = static_cast<uint32_t>(V - 1);  // (never used: need <= matches)
+  constexpr int kSteps = 4;  // steps in flight per warp
+  for (int st0 = warp; st0 < nst; st0 += kSteps * kWarpsF) {
+    uint4 r[kSteps];
+#pragma unroll
+    for (int u = 0; u < kSteps; ++u)
+      r[u] = st0 + u * kWarpsF < nst ? load_lane(st0 + u * kWarpsF) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < kSteps; ++u) {
+      const int st = st0 + u * kWarpsF;
+      if (st < nst) {  // warp-uniform
+        const unsigned n = __reduce_add_sync(0xffffffffu, count_lane(st, r[u]));
+        if (lane == 0) s.steps[st] = n;
+      }
+    }
+  }
+  __syncthreads();
+  pick(s, nst, false, need, [&](int e) -> unsigned long long { return s.steps[e]; });
+  __syncthreads();
+  if (warp == 0) {  // the token inside the picked step
+    const int st = static_cast<int>(s.r_u[1]);
+    const int e0 = st * step + lane * VN;
+    const uint4 rv = load_lane(st);
+    const unsigned n = count_lane(st, rv);
+    unsigned incl = n;
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+      const unsigned t = __shfl_up_sync(0xffffffffu, incl, o2);
+      if (lane >= o2) incl += t;
+    }
+    const unsigned long long before = s.r_m[0] + (incl - n);
+    if (n > 0 && before < need && need <= before + n) {
+      unsigned long long r = before;
+      for (int i = 0; i < VN && e0 + i < V; ++i) {
+        const uint32_t raw = (vec && e0 + VN <= V) ? Bits<T>::lane(rv, i) : Bits<T>::raw(x + e0 + i);
+        const uint32_t key = nkey<T>(raw);
+        if (key == tkey && pred(key, e0 + i) && ++r == need) {
+          s.r_u[2] = static_cast<uint32_t>(e0 + i);
+          break;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int idx = static_cast<int>(s.r_u[2]);
+  __syncthreads();
+  return idx;
+}
+
+// Radix selection path (fp32 rows, and bf16 rows whose value histogram would overflow): the
+// row's keep bound, returned to every thread.  Kept out of line so that its register pressure
+// does not spill into the histogram path.
+template <typename T>
+__device__ __noinline__ uint2 radix_bound(const T* x, int V, bool vec, Shared& s, float c2,
+                                          int top_k, float top_p, bool use_k, bool use_p) {
+  constexpr int KB = Bits<T>::K;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto all = [](uint32_t, int) { return true; };
+  // Highest score: the offset of the masses; a NaN or +inf row keeps everything (verification
+  // reports such rows as invalid).
+  uint32_t km = 0;
+  visit_row(x, V, vec, [&](int, uint32_t raw) { km = max(km, nkey<T>(raw)); });
+  km = block_max(km, s);
+  const float vmax = Bits<T>::value(nraw<T>(km));
+  const bool finite_max = vmax == vmax && vmax != INFINITY && vmax != -INFINITY;
+  if (!finite_max) return make_uint2(0u, static_cast<uint32_t>(INT_MAX));  // keep all
+  const float o = ceilf(vmax * c2);
+  auto weight = [&](uint32_t raw) -> unsigned long long {
+    const float w = ex2(fmaf(Bits<T>::value(raw), c2, -o));
+    return __float2ull_rz(w * kFixedScale);
+  };
+
+  uint32_t kkey = 0;
+  int kidx = INT_MAX;
+  auto in_k = [&](uint32_t key, int v) { return key > kkey || (key == kkey && v <= kidx); };
+
+  // Radix selection over the keys passing `pred`, by counts or masses, from the top: bf16 keys
+  // in levels of 11 and 5 bits, fp32 keys 11 + 11 + 10.  Counts and the four 11-bit parts of
+  // the masses go to the shared histogram with 32-bit atomics (integer sums: the result does
+  // not depend on their order).  With `p_of_total` the target is that fraction of the first
+  // level's total (top-p).  Returns the final key; `rest` receives the target left for the ties
+  // on that key.
+  auto select = [&](bool mass, unsigned long long target, float p_of_total, auto pred,
+                    unsigned long long& rest) {
+    uint32_t pre = 0;
+    int done = 0;  // key bits fixed so far
+    for (int l = 0; l < (KB == 16 ? 2 : 3); ++l) {
+      const int bits = KB == 16 ? (l == 0 ? 11 : 5) : (l == 2 ? 10 : 11);
+      const int nb = 1 << bits, sh = KB - done - bits;
+      for (int i = tid; i < nb; i += kFThreads) {
+        s.cnt[i] = 0u;
+#pragma unroll
+        for (int k = 0; k < kParts; ++k) s.part[k][i] = 0u;
+      }
+      __syncthreads();
+      visit_row(x, V, vec, [&](int i, uint32_t raw) {
+        const uint32_t key = nkey<T>(raw);
+        if ((done == 0 || (key >> (sh + bits)) == pre) && pred(key, i)) {
+          const int bin = static_cast<int>((key >> sh) & static_cast<uint32_t>(nb - 1));
+          if (mass) {
+            const unsigned long long w = weight(raw);
+#pragma unroll
+            for (int k = 0; k < kParts; ++k) {
+              // the top part also holds bit 44 (a mass of exactly 1): at most 2^11 per token
+              const uint32_t pk = static_cast<uint32_t>(k == kParts - 1 ? (w >> (11 * k)) : ((w >> (11 * k)) & 0x7ffull));
+              if (pk) atomicAdd(&s.part[k][bin], pk);
+            }
+          } else {
+            atomicAdd(&s.cnt[bin], 1u);
+          }
+        }
+      });
+      __syncthreads();
+      auto bin_mass = [&](int e) -> unsigned long long {
+        unsigned long long m = 0;
+#pragma unroll
+        for (int k = 0; k < kParts; ++k) m += static_cast<unsigned long long>(s.part[k][e]) << (11 * k);
+        return m;
+      };
+      if (l == 0 && p_of_total < 1.f) {  // top-p: keep while mass before < ceil(p * total)
+        unsigned long long t = 0;
+        for (int i = tid; i < nb; i += kFThreads) t += bin_mass(i);
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o2);
+        if (lane == 0) s.wmass[warp] = t;
+        __syncthreads();
+        if (tid == 0) {
+          unsigned long long tt = 0;
+          for (int w = 0; w < kWarpsF; ++w) tt += s.wmass[w];
+          const unsigned long long tg =
+              static_cast<unsigned long long>(ceil(static_cast<double>(p_of_total) * static_cast<double>(tt)));
+          s.r_m[1] = tg == 0 ? 1 : tg;
+        }
+        __syncthreads();
+        target = s.r_m[1];
+      }
+      pick(s, nb, true, target, [&](int e) -> unsigned long long {
+        return mass ? bin_mass(e) : static_cast<unsigned long long>(s.cnt[e]);
+      });
+      __syncthreads();
+      pre = (pre << bits) | s.r_u[1];
+      target -= s.r_m[0];
+      done += bits;
+      __syncthreads();
+    }
+    rest = target;
+    return pre;
+  };
+
+  if (use_k) {
+    unsigned long long rest = 0;
+    const uint32_t key = select(false, static_cast<unsigned long long>(top_k), 1.f, all, rest);
+    kidx = nth_index<T>(x, V, vec, s, key, rest, all);
+    kkey = key;
+  }
+  uint32_t fkey = kkey;
+  int fidx = kidx;
+  if (use_p) {
+    // The token where the mass before it (within the top-k set, or the row) stops being below
+    // top_p of that set's total.
+    unsigned long long rest = 0;
+    const uint32_t key = select(true, 1ull, top_p, in_k, rest);
+    // Inside the final key every kept token weighs the same w: the m-th one (index order) is
+    // the last kept, m = ceil(rest / w).
+    const unsigned long long w = weight(nraw<T>(key));
+    const unsigned long long m = w > 0 ? (rest + w - 1) / w : 1;
+    fidx = nth_index<T>(x, V, vec, s, key, m < 1 ? 1 : m, in_k);
+    fkey = key;
+  }
+  return make_uint2(score_key(Bits<T>::value(nraw<T>(fkey))), static_cast<uint32_t>(fidx));
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kFThreads, 1) filter_kernel(const FilterArgs A) {
-  extern __shared__ __align__(16) char smem_raw[];
+  extern __shared__ __align__(128) char smem_raw[];
   Shared& s = *reinterpret_cast<Shared*>(smem_raw);
-  constexpr int KB = Bits<T>::K, VN = Bits<T>::VN;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Q = 2 * A.D + 1, V = A.V;
   const long long rows = static_cast<long long>(A.B) * Q;
@@ -208,183 +432,176 @@ __global__ void __launch_bounds__(kFThreads, 1) filter_kernel(const FilterArgs A
       continue;
     }
     const bool vec = (reinterpret_cast<uintptr_t>(x) % 16) == 0;
-    // Highest score: the offset of the masses; a NaN or +inf row keeps everything (verification
-    // reports such rows as invalid).
-    uint32_t km = 0;
-    visit_row(x, V, vec, [&](int, uint32_t raw) { km = max(km, nkey<T>(raw)); });
-    km = block_max(km, s);
-    const float vmax = Bits<T>::value(nraw<T>(km));
-    const bool finite_max = vmax == vmax && vmax != INFINITY && vmax != -INFINITY;
-    if (!finite_max) {
-      if (tid == 0) A.bounds[row] = bound;
-      continue;
-    }
-    const float o = ceilf(vmax * A.c2);
-    auto weight = [&](uint32_t raw) -> unsigned long long {
-      const float w = ex2(fmaf(Bits<T>::value(raw), A.c2, -o));
-      return __float2ull_rz(w * kFixedScale);
-    };
-
-    uint32_t kkey = 0;
-    int kidx = INT_MAX;
-    auto in_k = [&](uint32_t key, int v) { return key > kkey || (key == kkey && v <= kidx); };
     auto all = [](uint32_t, int) { return true; };
 
-    // Radix selection over the keys passing `pred`, by counts or masses, from the top: bf16 keys
-    // in levels of 11 and 5 bits, fp32 keys 11 + 11 + 10.  Counts and the four 11-bit parts of
-    // the masses go to the shared histogram with 32-bit atomics (integer sums: the result does
-    // not depend on their order).  With `p_of_total` the target is that fraction of the first
-    // level's total (top-p).  Returns the final key; `rest` receives the target left for the ties
-    // on that key.
-    auto select = [&](bool mass, unsigned long long target, float p_of_total, auto pred,
-                      unsigned long long& rest) {
-      uint32_t pre = 0;
-      int done = 0;  // key bits fixed so far
-      for (int l = 0; l < (KB == 16 ? 2 : 3); ++l) {
-        const int bits = KB == 16 ? (l == 0 ? 11 : 5) : (l == 2 ? 10 : 11);
-        const int nb = 1 << bits, sh = KB - done - bits;
-        for (int i = tid; i < nb; i += kFThreads) {
-          s.cnt[i] = 0u;
-#pragma unroll
-          for (int k = 0; k < kParts; ++k) s.part[k][i] = 0u;
-        }
-        __syncthreads();
-        visit_row(x, V, vec, [&](int i, uint32_t raw) {
-          const uint32_t key = nkey<T>(raw);
-          if ((done == 0 || (key >> (sh + bits)) == pre) && pred(key, i)) {
-            const int bin = static_cast<int>((key >> sh) & static_cast<uint32_t>(nb - 1));
-            if (mass) {
-              const unsigned long long w = weight(raw);
-#pragma unroll
-              for (int k = 0; k < kParts; ++k) {
-                // the top part also holds bit 44 (a mass of exactly 1): at most 2^11 per token
-                const uint32_t pk = static_cast<uint32_t>(k == kParts - 1 ? (w >> (11 * k)) : ((w >> (11 * k)) & 0x7ffull));
-                if (pk) atomicAdd(&s.part[k][bin], pk);
-              }
-            } else {
-              atomicAdd(&s.cnt[bin], 1u);
-            }
-          }
-        });
-        __syncthreads();
-        auto bin_mass = [&](int e) -> unsigned long long {
-          unsigned long long m = 0;
-#pragma unroll
-          for (int k = 0; k < kParts; ++k) m += static_cast<unsigned long long>(s.part[k][e]) << (11 * k);
-          return m;
-        };
-        if (l == 0 && p_of_total < 1.f) {  // top-p: keep while mass before < ceil(p * total)
+    if constexpr (Bits<T>::K == 16) {
+      // bf16: a count per score value (65536 of them, 16-bit counters two to a word) from one
+      // read of the row; the highest score, the top-k cut and the top-p cut follow from the
+      // counts and the per-value weights, exactly as from the tokens themselves.  A counter that
+      // would pass 65535 sends the row to the radix selection below.
+      uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw + kHistOffset);
+      uint4* h4 = reinterpret_cast<uint4*>(hist);
+      for (int i = tid; i < kHistWords / 4; i += kFThreads) h4[i] = make_uint4(0u, 0u, 0u, 0u);
+      __syncthreads();
+      visit_row<T, 4>(x, V, vec, [&](int, uint32_t raw) {
+        const uint32_t key = nkey<T>(raw);
+        atomicAdd(&hist[key >> 1], 1u << ((key & 1u) << 4));
+      });
+      __syncthreads();
+      auto cnt = [&](uint32_t key) -> uint32_t {
+        return (hist[key >> 1] >> ((key & 1u) << 4)) & 0xffffu;
+      };
+      // The 65536 keys in kFThreads chunks of kChunk, totals in s.ctot (key order).  For masses
+      // (an exp2 per populated key) chunk c is summed by warp c mod kWarpsF, its lanes on
+      // consecutive words, so the few chunks that hold the row's values are spread over all warps.
+      constexpr int kChunk = 65536 / kFThreads;
+      auto chunk_totals = [&](auto val_pair) {
+        for (int c = warp; c < kFThreads; c += kWarpsF) {
           unsigned long long t = 0;
-          for (int i = tid; i < nb; i += kFThreads) t += bin_mass(i);
+#pragma unroll
+          for (int h = 0; h < kChunk / 64; ++h) {
+            const uint32_t w = static_cast<uint32_t>(c * (kChunk / 2) + h * 32 + lane);
+            t += val_pair(w);
+          }
 #pragma unroll
           for (int o2 = 16; o2 > 0; o2 >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o2);
-          if (lane == 0) s.wmass[warp] = t;
-          __syncthreads();
-          if (tid == 0) {
-            unsigned long long tt = 0;
-            for (int w = 0; w < kWarpsF; ++w) tt += s.wmass[w];
-            const unsigned long long tg =
-                static_cast<unsigned long long>(ceil(static_cast<double>(p_of_total) * static_cast<double>(tt)));
-            s.r_m[1] = tg == 0 ? 1 : tg;
-          }
-          __syncthreads();
-          target = s.r_m[1];
+          if (lane == 0) s.ctot[c] = t;
         }
-        pick(s, nb, true, target, [&](int e) -> unsigned long long {
-          return mass ? bin_mass(e) : static_cast<unsigned long long>(s.cnt[e]);
-        });
-        __syncthreads();
-        pre = (pre << bits) | s.r_u[1];
-        target -= s.r_m[0];
-        done += bits;
-        __syncthreads();
-      }
-      rest = target;
-      return pre;
-    };
-    // The need-th (1-based) token in index order among those with key == tkey passing `pred`:
-    // every warp counts the matches of whole steps of 32*VN consecutive elements (16-byte loads),
-    // a prefix over the steps picks one, and warp 0 finds the token inside it.
-    auto nth_index = [&](uint32_t tkey, unsigned long long need, auto pred) {
-      const int step = 32 * VN;
-      const int nst = (V + step - 1) / step;
-      auto count_lane = [&](int st, uint32_t* raws) {
-        const int e0 = st * step + lane * VN;
-        if (vec && e0 + VN <= V) {
-          const uint4 r = *reinterpret_cast<const uint4*>(x + e0);
-#pragma unroll
-          for (int i = 0; i < VN; ++i) raws[i] = Bits<T>::lane(r, i);
-        } else {
-#pragma unroll
-          for (int i = 0; i < VN; ++i) raws[i] = e0 + i < V ? Bits<T>::raw(x + e0 + i) : 0u;
-        }
-        unsigned n = 0;
-#pragma unroll
-        for (int i = 0; i < VN; ++i) {
-          const uint32_t key = nkey<T>(raws[i]);
-          if (e0 + i < V && key == tkey && pred(key, e0 + i)) ++n;
-        }
-        return n;
       };
-      if (tid == 0) s.r_u[2] = static_cast<uint32_t>(V - 1);  // (never used: need <= matches)
-      for (int st = warp; st < nst; st += kWarpsF) {
-        uint32_t raws[VN];
-        const unsigned n = __reduce_add_sync(0xffffffffu, count_lane(st, raws));
-        if (lane == 0) s.steps[st] = n;
-      }
-      __syncthreads();
-      pick(s, nst, false, need, [&](int e) -> unsigned long long { return s.steps[e]; });
-      __syncthreads();
-      if (warp == 0) {
-        const int st = static_cast<int>(s.r_u[1]);
-        uint32_t raws[VN];
-        const unsigned n = count_lane(st, raws);
-        unsigned incl = n;
-#pragma unroll
-        for (int o2 = 1; o2 < 32; o2 <<= 1) {
-          const unsigned t = __shfl_up_sync(0xffffffffu, incl, o2);
-          if (lane >= o2) incl += t;
+      // Counts (cheap) per thread over its own chunk, from word (lane + i) mod 64 so that the
+      // 32 lanes of a warp read 32 different banks.
+      uint32_t km = 0;
+      unsigned long long tc = 0;
+      {
+        const uint32_t k0 = static_cast<uint32_t>(tid) * kChunk;
+        const uint32_t* hw = hist + (k0 >> 1);
+        for (int i = 0; i < kChunk / 2; ++i) {
+          const uint32_t w = static_cast<uint32_t>((i + lane) & (kChunk / 2 - 1));
+          const uint32_t v = hw[w];
+          tc += (v & 0xffffu) + (v >> 16);
+          if (v >> 16) km = max(km, k0 + 2 * w + 1);
+          else if (v) km = max(km, k0 + 2 * w);
         }
-        const unsigned long long before = s.r_m[0] + (incl - n);
-        if (n > 0 && before < need && need <= before + n) {
-          unsigned long long r = before;
-          const int e0 = st * step + lane * VN;
-          for (int i = 0; i < VN; ++i) {
-            const uint32_t key = nkey<T>(raws[i]);
-            if (e0 + i < V && key == tkey && pred(key, e0 + i) && ++r == need) {
-              s.r_u[2] = static_cast<uint32_t>(e0 + i);
-              break;
+        s.ctot[tid] = tc;
+      }
+      // A counter that passed 65535 lost 65535 (or, carried out of its word, 65536) counts, so
+      // the counts add up to V exactly when none overflowed.
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) tc += __shfl_xor_sync(0xffffffffu, tc, o2);
+      if (lane == 0) s.wmass[warp] = tc;
+      __syncthreads();
+      if (tid == 0) {
+        unsigned long long t = 0;
+        for (int w = 0; w < kWarpsF; ++w) t += s.wmass[w];
+        s.ovf = t != static_cast<unsigned long long>(V);
+      }
+      km = block_max(km, s);  // (its barriers also publish s.ovf)
+      if (!s.ovf) {
+        const float vmax = Bits<T>::value(nraw<T>(km));
+        if (!(vmax == vmax && vmax != INFINITY && vmax != -INFINITY)) {
+          if (tid == 0) A.bounds[row] = bound;  // keep all (verification reports the row)
+          __syncthreads();
+          continue;
+        }
+        const float o = ceilf(vmax * A.c2);
+        auto wgt = [&](uint32_t key) -> unsigned long long {
+          const float w = ex2(fmaf(Bits<T>::value(nraw<T>(key)), A.c2, -o));
+          return __float2ull_rz(w * kFixedScale);
+        };
+        // Warp 0 walks chunk e from its highest key down, starting with `run` above it, to the
+        // key where the running total reaches `target`; r_u[2] = that key, r_m[1] = the target
+        // left for it.
+        auto walk = [&](int e, unsigned long long run, unsigned long long target, auto val) {
+          if (warp == 0) {
+            unsigned long long v[kChunk / 32], t = 0;
+#pragma unroll
+            for (int i = 0; i < kChunk / 32; ++i) {
+              v[i] = val(static_cast<uint32_t>(e * kChunk + kChunk - 1 - (lane * (kChunk / 32) + i)));
+              t += v[i];
+            }
+            unsigned long long incl = t;
+#pragma unroll
+            for (int o2 = 1; o2 < 32; o2 <<= 1) {
+              const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o2);
+              if (lane >= o2) incl += y;
+            }
+            const unsigned long long before = run + incl - t;
+            const unsigned mine = __ballot_sync(0xffffffffu, before < target && target <= run + incl);
+            const int owner = mine ? __ffs(static_cast<int>(mine)) - 1 : 31;
+            if (lane == owner) {
+              unsigned long long r = before;
+              int i = 0;
+              for (; i < kChunk / 32 - 1; ++i) {
+                if (r + v[i] >= target) break;
+                r += v[i];
+              }
+              s.r_u[2] = static_cast<uint32_t>(e * kChunk + kChunk - 1 - (lane * (kChunk / 32) + i));
+              s.r_m[1] = target - r;
             }
           }
+          __syncthreads();
+        };
+        uint32_t K = 0, kk = 0;
+        unsigned long long need = 1, krest = 0;
+        if (use_k) {
+          pick(s, kFThreads, true, static_cast<unsigned long long>(A.top_k),
+               [&](int e) -> unsigned long long { return s.ctot[e]; });
+          __syncthreads();
+          walk(static_cast<int>(s.r_u[1]), s.r_m[0], static_cast<unsigned long long>(A.top_k),
+               [&](uint32_t key) -> unsigned long long { return cnt(key); });
+          kk = s.r_u[2];
+          krest = s.r_m[1];
+          K = kk;
+          need = krest;
+          __syncthreads();
         }
+        if (use_p) {
+          // masses within the top-k set: of the boundary key only its first krest tokens count
+          auto mass_of = [&](uint32_t key) -> unsigned long long {
+            unsigned long long c = cnt(key);
+            if (use_k) {
+              if (key < kk) return 0ull;
+              if (key == kk) c = krest;
+            }
+            return c ? c * wgt(key) : 0ull;
+          };
+          chunk_totals([&](uint32_t w) -> unsigned long long {
+            return mass_of(2 * w) + mass_of(2 * w + 1);
+          });
+          __syncthreads();
+          if (warp == 0) {
+            unsigned long long t = 0;
+            for (int e = lane; e < kFThreads; e += 32) t += s.ctot[e];
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o2);
+            if (lane == 0) {
+              const unsigned long long tg = static_cast<unsigned long long>(
+                  ceil(static_cast<double>(A.top_p) * static_cast<double>(t)));
+              s.r_m[1] = tg == 0 ? 1 : tg;
+            }
+          }
+          __syncthreads();
+          const unsigned long long target = s.r_m[1];
+          __syncthreads();
+          pick(s, kFThreads, true, target, [&](int e) -> unsigned long long { return s.ctot[e]; });
+          __syncthreads();
+          walk(static_cast<int>(s.r_u[1]), s.r_m[0], target, mass_of);
+          K = s.r_u[2];
+          const unsigned long long rest = s.r_m[1];
+          __syncthreads();
+          // inside key K every token weighs the same w: the m-th one (index order) is the last
+          const unsigned long long w = wgt(K);
+          const unsigned long long mm = w > 0 ? (rest + w - 1) / w : 1;
+          need = mm < 1 ? 1 : mm;
+        }
+        const int idx = nth_index<T>(x, V, vec, s, K, need, all);
+        bound = make_uint2(score_key(Bits<T>::value(nraw<T>(K))), static_cast<uint32_t>(idx));
+        if (tid == 0) A.bounds[row] = bound;
+        __syncthreads();
+        continue;
       }
-      __syncthreads();
-      const int idx = static_cast<int>(s.r_u[2]);
-      __syncthreads();
-      return idx;
-    };
-
-    if (use_k) {
-      unsigned long long rest = 0;
-      const uint32_t key = select(false, static_cast<unsigned long long>(A.top_k), 1.f, all, rest);
-      kidx = nth_index(key, rest, all);
-      kkey = key;
     }
-    uint32_t fkey = kkey;
-    int fidx = kidx;
-    if (use_p) {
-      // The token where the mass before it (within the top-k set, or the row) stops being below
-      // top_p of that set's total.
-      unsigned long long rest = 0;
-      const uint32_t key = select(true, 1ull, A.top_p, in_k, rest);
-      // Inside the final key every kept token weighs the same w: the m-th one (index order) is
-      // the last kept, m = ceil(rest / w).
-      const unsigned long long w = weight(nraw<T>(key));
-      const unsigned long long m = w > 0 ? (rest + w - 1) / w : 1;
-      fidx = nth_index(key, m < 1 ? 1 : m, in_k);
-      fkey = key;
-    }
-    bound = make_uint2(score_key(Bits<T>::value(nraw<T>(fkey))), static_cast<uint32_t>(fidx));
+    bound = radix_bound<T>(x, V, vec, s, A.c2, A.top_k, A.top_p, use_k, use_p);
     if (tid == 0) A.bounds[row] = bound;
     __syncthreads();
   }
@@ -426,7 +643,9 @@ extern "C" int specdec_sampling_filter(const void* target_logits, const void* dr
   A.status = dev_status;
   const long long rows = static_cast<long long>(B) * (2 * D + 1);
   const int grid = static_cast<int>(std::min<long long>(rows, sms));
-  const int smem = static_cast<int>(sizeof(Shared));
+  const int smem = dtype == SPECDEC_BF16
+                       ? static_cast<int>(kHistOffset) + kHistWords * static_cast<int>(sizeof(uint32_t))
+                       : static_cast<int>(sizeof(Shared));
   static bool attr_set[2][64] = {{false}};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SPECDEC_ERR_CUDA;

@@ -177,6 +177,30 @@ __device__ __forceinline__ void fold4(const uint4* r, float c2, float& o, float&
   }
 }
 
+// fold4 for four vectors already unpacked (and masked) into floats.
+template <int VN>
+__device__ __forceinline__ void fold4f(const float (&x)[4][VN], float c2, float& o, float& s) {
+  float t[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float e[VN];
+#pragma unroll
+    for (int i = 0; i < VN; ++i) e[i] = ex2(fmaf(x[k][i], c2, -o));
+#pragma unroll
+    for (int w = VN / 2; w > 0; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) e[i] += e[i + w];
+    t[k] = e[0];
+  }
+  const float v = (t[0] + t[1]) + (t[2] + t[3]);
+  if (v <= kRescale) {
+    s += v;
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) fold<VN>(x[k], c2, o, s);
+  }
+}
+
 template <typename T, bool kVec>
 __device__ __forceinline__ void load_row_slice(const T* row, int e, int s1, uint4& buf) {
   constexpr int VN = Vec<T>::N;
@@ -211,15 +235,23 @@ struct SampleArgs {
   int32_t* status;
 };
 
-// Order-preserving code of a float score (-0 counted as +0), and the keep test of a token with
-// score x at index v against its row's bound (key, index).
-__device__ __forceinline__ uint32_t score_key(float f) {
-  const uint32_t u = (f == 0.f) ? 0u : __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+// A row's keep bound (order-preserving 32-bit key of the last kept score, its index) as a float
+// threshold: a token with score x at index v is kept iff x > t, or x == t and v <= ti.  Keys at
+// or below the key of -inf (-inf itself, negative NaN patterns) give t = -inf.  The test keeps
+// NaN (it is never below t), so a NaN score still makes its row invalid.
+struct KeepF {
+  float t;
+  int ti;
+};
+__device__ __forceinline__ KeepF keep_threshold(uint2 bd) {
+  constexpr uint32_t kNegInfKey = 0x007fffffu;  // key of -inf: ~0xff800000
+  if (bd.x < kNegInfKey) return {kNegInf, 0x7fffffff};
+  if (bd.x == kNegInfKey) return {kNegInf, static_cast<int>(bd.y)};
+  const uint32_t u = (bd.x & 0x80000000u) ? (bd.x & 0x7fffffffu) : ~bd.x;
+  return {__uint_as_float(u), static_cast<int>(bd.y)};
 }
-__device__ __forceinline__ bool kept(uint2 bd, float x, int v) {
-  const uint32_t k = score_key(x);
-  return k > bd.x || (k == bd.x && v <= static_cast<int>(bd.y));
+__device__ __forceinline__ float masked(const KeepF& k, float x, int v) {
+  return (!(x < k.t) && (x != k.t || v <= k.ti)) ? x : kNegInf;
 }
 
 template <typename T, bool kVec, int W>
@@ -243,7 +275,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
   __shared__ int s_a, s_bad, s_found, s_y, s_last, s_fail;
   __shared__ __align__(8) uint64_t full[kMaxRingStages], empty[kMaxRingStages], pbar;
   __shared__ StreamPlan plan;
-  __shared__ uint2 s_keep[kMaxQ];            // the rows' keep bounds (sampling settings)
+  __shared__ KeepF s_keep[kMaxQ];            // the rows' keep thresholds (sampling settings)
   __shared__ int pre_d[SPECDEC_MAX_DRAFT];   // fetched while the slice streams
   __shared__ float pre_u[SPECDEC_MAX_DRAFT + 1], pre_z[SPECDEC_MAX_DRAFT], pre_w[SPECDEC_MAX_DRAFT];
 
@@ -292,7 +324,8 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
   }
   const bool filter = A.keep != nullptr;
   for (int k = tid; k < Q; k += kThreads)
-    s_keep[k] = filter ? A.keep[static_cast<long long>(b) * Q + k] : make_uint2(0u, 0x7fffffffu);
+    s_keep[k] = keep_threshold(filter ? A.keep[static_cast<long long>(b) * Q + k]
+                                      : make_uint2(0u, 0x7fffffffu));
   if (tid == 0) {
     s_bad = 0;
     s_found = 0;
@@ -359,13 +392,26 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
             const int nv = n / VN;
             int v = tid;
             if (filter) {  // sampling settings: tokens outside the row's kept set weigh 0
-              const uint2 bd = s_keep[q];
+              const KeepF kf = s_keep[q];
+              for (; v + 3 * kConsumers < nv; v += 4 * kConsumers) {
+                uint4 r[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) r[k] = v4[v + k * kConsumers];
+                float x[4][VN];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  Vec<T>::unpack(r[k], x[k]);
+                  const int e0 = v0 + (v + k * kConsumers) * VN;
+#pragma unroll
+                  for (int i = 0; i < VN; ++i) x[k][i] = masked(kf, x[k][i], e0 + i);
+                }
+                fold4f<VN>(x, c2, o, s);
+              }
               for (; v < nv; v += kConsumers) {
                 float x[VN];
                 Vec<T>::unpack(v4[v], x);
 #pragma unroll
-                for (int i = 0; i < VN; ++i)
-                  if (!kept(bd, x[i], v0 + v * VN + i)) x[i] = kNegInf;
+                for (int i = 0; i < VN; ++i) x[i] = masked(kf, x[i], v0 + v * VN + i);
                 fold<VN>(x, c2, o, s);
               }
               return;
@@ -396,8 +442,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
       const T* row = row_ptr(q);
       float o = kOffsetNone, s = 0.f;
       for (int e = s0 + tid; e < s1; e += kConsumers) {
-        float x = Vec<T>::scalar(row + e);
-        if (!kept(s_keep[q], x, e)) x = kNegInf;
+        float x = masked(s_keep[q], Vec<T>::scalar(row + e), e);
         fold<1>(&x, c2, o, s);
       }
       warp_merge(o, s);
@@ -412,8 +457,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
     if (lane == kWarps && kVec) {  // elements past the streamed body (fewer than one vector)
       const T* row = row_ptr(q);
       for (int e = tail_from; e < s1; ++e) {
-        float x = Vec<T>::scalar(row + e);
-        if (!kept(s_keep[q], x, e)) x = kNegInf;
+        float x = masked(s_keep[q], Vec<T>::scalar(row + e), e);
         fold<1>(&x, c2, o, s);
       }
     }
@@ -453,8 +497,8 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
         accept = false;
       } else {
         // A draft outside a row's kept set has probability 0 there.
-        const float z = kept(s_keep[lane], pre_z[lane], d) ? pre_z[lane] : kNegInf;
-        const float w = kept(s_keep[D + 1 + lane], pre_w[lane], d) ? pre_w[lane] : kNegInf;
+        const float z = masked(s_keep[lane], pre_z[lane], d);
+        const float w = masked(s_keep[D + 1 + lane], pre_w[lane], d);
         if (w == kNegInf) {
           accept = true;  // q(d) = 0
         } else {
@@ -535,9 +579,9 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
   const float ow = resid ? go[D + 1 + a] : 0.f;
   const float iw = s_iw;
   bool use_p = !resid;
-  const uint2 kz = s_keep[a], kw = s_keep[resid ? D + 1 + a : a];
-  auto zmask = [&](float x, int i) { return kept(kz, x, s0 + i) ? x : kNegInf; };
-  auto wmask = [&](float x, int i) { return kept(kw, x, s0 + i) ? x : kNegInf; };
+  const KeepF kz = s_keep[a], kw = s_keep[resid ? D + 1 + a : a];
+  auto zmask = [&](float x, int i) { return masked(kz, x, s0 + i); };
+  auto wmask = [&](float x, int i) { return masked(kw, x, s0 + i); };
   auto r_at = [&](int i) -> float {
     const float p = ex2(fmaf(zmask(Vec<T>::scalar(zs + i), i), c2, -oz)) * iz;
     if (use_p) return p;

@@ -291,9 +291,11 @@ class SequencePool:
         self.out_token = torch.zeros(S, **i32)
         self.status = torch.zeros(1, **i32)
         self.workspaces = Workspaces(dev)
-        # schedule readback: counts | offsets | uniform | finished | reason (int32 each)
-        self._host = torch.zeros(4 + (S + 1) + 3 * S, dtype=torch.int32).pin_memory()
+        # schedule readback: counts | offsets | uniform | finished | reason | slot_len | perm
+        self._host = torch.zeros(4 + (S + 1) + 5 * S, dtype=torch.int32).pin_memory()
         self._dev_rb = torch.zeros_like(self._host, device=dev)
+        self.host_len = [0] * S           # slot lengths as of the last schedule
+        self.host_perm = []               # the last schedule's slots in batch order
         self.taken = [False] * S          # admitted and not yet reported finished
         self.run_of = [None] * S          # arena run of each taken slot
 
@@ -346,7 +348,8 @@ class SequencePool:
         """Schedule the round on the device and read it back once.  Returns (batches, finished):
         batches as (offset, rows, uniform) into ``perm``; finished as (slot, reason) -- those
         slots' tokens stay readable (``tokens``) until they are admitted again, and their arena
-        runs are returned to the allocator now."""
+        runs are returned to the allocator now.  ``host_len`` receives every slot's length and
+        ``host_perm`` the scheduled slots in batch order."""
         specdec.pool_schedule(self.slot_state, self.slot_len, self.bs, self.window, self.perm,
                               self.offsets, self.uniform, self.finished, self.reason, self.counts,
                               self.status, stream)
@@ -356,6 +359,8 @@ class SequencePool:
         rb[5 + S:5 + 2 * S].copy_(self.uniform, non_blocking=True)
         rb[5 + 2 * S:5 + 3 * S].copy_(self.finished, non_blocking=True)
         rb[5 + 3 * S:5 + 4 * S].copy_(self.reason, non_blocking=True)
+        rb[5 + 4 * S:5 + 5 * S].copy_(self.slot_len, non_blocking=True)
+        rb[5 + 5 * S:5 + 6 * S].copy_(self.perm, non_blocking=True)
         self._host.copy_(rb, non_blocking=True)
         (stream or torch.cuda.current_stream()).synchronize()
         h = self._host.tolist()
@@ -363,6 +368,8 @@ class SequencePool:
         off = h[4:5 + S]
         uni = h[5 + S:5 + 2 * S]
         fin = list(zip(h[5 + 2 * S:5 + 2 * S + nf], h[5 + 3 * S:5 + 3 * S + nf]))
+        self.host_len = h[5 + 4 * S:5 + 5 * S]
+        self.host_perm = h[5 + 5 * S:5 + 5 * S + h[2]]
         for s, _ in fin:
             self.alloc.free(self.run_of[s])
             self.taken[s] = False

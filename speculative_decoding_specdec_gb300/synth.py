@@ -72,16 +72,24 @@ def greedy_round(gen, B, D, V, alpha, dtype=torch.bfloat16, device="cpu", row_st
 
 
 def sampled_round(gen, B, D, V, temperature, sigma=0.5, dtype=torch.bfloat16, device="cpu",
-                  row_stride=None):
+                  row_stride=None, draft_candidates=0):
     """Target scores [B, D+1, V], draft-model scores [B, D, V] = target + N(0, sigma^2), drafts
-    drawn from the draft model's softmax at ``temperature``, and uniforms [B, D+1] in [0, 1)."""
+    drawn from the draft model's softmax at ``temperature``, and uniforms [B, D+1] in [0, 1).
+    With ``draft_candidates`` = k (0 < k < V) the draft model samples among its k highest scores
+    only, as a draft model run with a top-k setting does."""
     z = torch.randn(B, D + 1, V, generator=gen, device=device, dtype=torch.float32)
     w = z[:, :D, :] + sigma * torch.randn(B, D, V, generator=gen, device=device,
                                           dtype=torch.float32)
     z = z.to(dtype)
     w = w.to(dtype)
-    q = torch.softmax(w.to(torch.float64) / temperature, dim=-1)
-    draft = torch.multinomial(q.reshape(B * D, V), 1, generator=gen).reshape(B, D)
+    if 0 < draft_candidates < V:
+        val, idx = torch.topk(w.to(torch.float64), draft_candidates, dim=-1)
+        qk = torch.softmax(val / temperature, dim=-1)
+        pick = torch.multinomial(qk.reshape(B * D, -1), 1, generator=gen).reshape(B, D)
+        draft = idx.gather(-1, pick[..., None])[..., 0]
+    else:
+        q = torch.softmax(w.to(torch.float64) / temperature, dim=-1)
+        draft = torch.multinomial(q.reshape(B * D, V), 1, generator=gen).reshape(B, D)
     uniforms = torch.rand(B, D + 1, generator=gen, device=device, dtype=torch.float32)
     return (_strided(z, row_stride), _strided(w, row_stride), draft.to(torch.int32), uniforms)
 

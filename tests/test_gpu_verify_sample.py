@@ -329,3 +329,38 @@ def test_filter_host_errors():
     for k, p in ((0, 0.0), (0, 1.5), (-1, 1.0)):
         with pytest.raises(sd.SpecdecError):
             sd.sampling_filter(tl.to(DEV), dl.to(DEV), 0.7, k, p, bounds, st)
+
+
+@pytest.mark.parametrize("ties,top_k,top_p", [
+    (65535, 1000, 1.0),      # a counter filled exactly: the histogram path, cut inside the ties
+    (65535, 0, 0.9),
+    (65536, 1000, 1.0),      # one more: the counter overflows, the row takes the radix path
+    (70000, 0, 0.9),
+    (70000, 100, 0.95),
+])
+def test_keep_bounds_many_equal_scores(ties, top_k, top_p):
+    """bf16 rows (V = 151552) whose highest score is shared by `ties` tokens at spread-out
+    indices: the value histogram holds up to 65535 equal scores; more send the row to the radix
+    selection.  Either way the kept set equals the oracle's."""
+    import speculative_decoding_specdec_gb300.specdec as sd
+    B, D, V = 1, 1, 151552
+    gen = synth.make_gen(77 + ties + top_k)
+    tl, dl, _, _ = synth.sampled_round(gen, B, D, V, 0.7, dtype=torch.bfloat16)
+    g = torch.Generator().manual_seed(ties)
+    for row in (tl[0, 0], tl[0, 1], dl[0, 0]):
+        idx = torch.randperm(V, generator=g)[:ties]
+        row[idx] = 8.0                                  # above every N(0,1) score
+    bounds = torch.zeros((B, 2 * D + 1, 2), dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sd.sampling_filter(tl.to(DEV), dl.to(DEV), 0.7, top_k, top_p, bounds, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    bnd = bounds.cpu().numpy().astype(np.int64)
+    rows = rows_of(tl.float().numpy(), dl.float().numpy())
+    for q in range(2 * D + 1):
+        got = kept_from_bounds(rows[0, q], bnd[0, q])
+        exp = O.sampling_keep(rows[0, q].astype(np.float64), 0.7, top_k, top_p)
+        if not np.array_equal(got, exp):   # top_p on a cumulative mass: either cut is exact
+            assert O.top_p_margin(rows[0, q].astype(np.float64), 0.7, top_k, top_p) < 2e-6, q
+            assert abs(int(got.sum()) - int(exp.sum())) == 1
+        assert 0 < got.sum() < ties
