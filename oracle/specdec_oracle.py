@@ -58,6 +58,11 @@ Readings where the pages leave a step open (each is listed again in the design doc):
   leftover.  w = 0 is the exact-length rule above.  Windowed batches come first, then the
   leftovers in (length, index) order cut into mixed batches.  Only a windowed batch of one length
   is flagged uniform (verified in place).
+* In-kernel uniforms (the fused round): u[b][j] for batch row b and j = 0..D is word j mod 4 of
+  Philox4x32-10 [Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+  SC11] at counter (j div 4, b, offset mod 2^32, offset div 2^32) and key (seed mod 2^32,
+  seed div 2^32), as (x >> 8) * 2^-24 (24 bits: exact in fp32 and fp64, in [0, 1)).  The caller
+  advances ``offset`` per round.
 * SequencePool lifecycle: a slot is FREE, ACTIVE, or FINISHED (by end-of-sequence token or by its
   length limit).  Only ACTIVE slots are grouped ("a pool of active sequences").  A sequence
   finishes at the first newly committed position q with token == eos_id or q + 1 == its length
@@ -93,6 +98,8 @@ __all__ = [
     "retire",
     "pool_admit",
     "FirstFitArena",
+    "philox",
+    "philox_uniforms",
 ]
 
 
@@ -636,3 +643,45 @@ class FirstFitArena:
             run = 0 if u else run + 1
             best = max(best, run)
         return best
+
+
+# --------------------------------------------------------------------------------------------
+# Counter-based uniforms for the fused round  [Philox, SC11 "Parallel Random Numbers: As Easy as
+# 1, 2, 3"; the uniforms u[b][j] of IE5 "Exactness Means Different Things..." drawn in-kernel]
+# --------------------------------------------------------------------------------------------
+
+def philox(ctr, key, bits: int = 32, rounds: int = 10):
+    """PhiloxNx W-R with N = 4 words of ``bits`` (32 or 64) bits: ``rounds`` rounds of
+    (hi0, lo0) = M0 * c0, (hi1, lo1) = M1 * c2, c = (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0),
+    the key bumped by the Weyl constants (W0, W1) between rounds."""
+    mask = (1 << bits) - 1
+    if bits == 32:
+        M = (0xD2511F53, 0xCD9E8D57)
+        W = (0x9E3779B9, 0xBB67AE85)
+    elif bits == 64:
+        M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)
+        W = (0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B)
+    else:
+        raise OracleError("word size")
+    c = [int(x) & mask for x in ctr]
+    k = [int(x) & mask for x in key]
+    for r in range(rounds):
+        if r:
+            k = [(k[0] + W[0]) & mask, (k[1] + W[1]) & mask]
+        p0 = M[0] * c[0]
+        p1 = M[1] * c[2]
+        c = [(p1 >> bits) ^ c[1] ^ k[0], p1 & mask, (p0 >> bits) ^ c[3] ^ k[1], p0 & mask]
+    return c
+
+
+def philox_uniforms(seed: int, offset: int, B: int, D: int):
+    """The uniforms u[B, D+1] of one round drawn from (seed, offset) as the fused round draws
+    them: u[b][j] = (x >> 8) * 2^-24, x = word j mod 4 of Philox4x32-10 at counter
+    (j div 4, b, offset mod 2^32, offset div 2^32), key (seed mod 2^32, seed div 2^32)."""
+    u = np.zeros((B, D + 1), dtype=np.float64)
+    key = (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
+    for b in range(B):
+        for j in range(D + 1):
+            x = philox((j // 4, b, offset & 0xFFFFFFFF, (offset >> 32) & 0xFFFFFFFF), key)[j % 4]
+            u[b, j] = (x >> 8) / float(1 << 24)
+    return u
