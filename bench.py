@@ -42,6 +42,13 @@ def parse():
                    help="sampled workloads: top-k sampling setting (0: off)")
     p.add_argument("--top-p", type=float, default=1.0,
                    help="sampled workloads: top-p sampling setting (1: off)")
+    p.add_argument("--launch", default="graph+pdl", choices=["stream", "pdl", "graph", "graph+pdl"],
+                   help="how the timed rounds are launched: plain stream launches; each "
+                        "realignment as a programmatic dependent of its verification (pdl); the "
+                        "timed rounds captured once into a CUDA graph and replayed (graph)")
+    p.add_argument("--philox", action="store_true",
+                   help="sampled workloads: draw the uniforms in-kernel (Philox) instead of "
+                        "reading them from HBM")
     p.add_argument("--window", type=int, default=0,
                    help="exspec_serving: length window of a batch (0: exact length)")
     p.add_argument("--ping-pong", action="store_true",
@@ -305,30 +312,67 @@ def run_specdec(args, rank, ws, local):
         d = drafts[r] if d is None else d
         if w.mode == "greedy":
             eng.verify_greedy(lg, d)
+        elif args.philox:
+            eng.verify_sample(lg, draft_logits[r], d, None, w.temperature,
+                              top_k=args.top_k, top_p=args.top_p, seed=w.seed)
         else:
             eng.verify_sample(lg, draft_logits[r], d, uniforms[r], w.temperature,
                               top_k=args.top_k, top_p=args.top_p)
 
     # ---------------- device-resident timing
-    eng.start(prompts)
-    for r in range(Wm):
-        verify(r)
-        eng.realign(drafts[r], copy_engine=args.copy_engine)
-    torch.cuda.synchronize()
+    # With --pdl each realignment is launched as a programmatic dependent of the verification
+    # ahead of it; with --graph the K timed rounds are captured once into a CUDA graph and the
+    # timed region is one replay.  Either way the timed rounds carry no events between their
+    # kernels (an event would serialise them), and a second pass over the same rounds, with
+    # events, gives the per-kernel times.
+    use_pdl = "pdl" in args.launch
+    eng.pdl = use_pdl
+    fused = args.launch != "stream"
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+
+    def warm():
+        eng.start(prompts)
+        for r in range(Wm):
+            verify(r)
+            eng.realign(drafts[r], copy_engine=args.copy_engine)
+        torch.cuda.synchronize()
+
+    def rounds(inner):
+        for i in range(K):
+            r = Wm + i
+            if inner:
+                ev[i][0].record(stream)
+            verify(r)
+            if inner:
+                ev[i][1].record(stream)
+            eng.realign(drafts[r], copy_engine=args.copy_engine)
+            if inner:
+                ev[i][2].record(stream)
+
+    warm()
+    graph = None
+    launch_used = args.launch
+    if args.launch.startswith("graph"):
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                rounds(False)
+            torch.cuda.synchronize()
+        except Exception as exc:  # capture refused: time the same rounds as stream launches
+            print(f"graph capture failed ({exc}); timing stream launches", file=sys.stderr)
+            graph = None
+            launch_used = "pdl" if use_pdl else "stream"
+            warm()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         t0.record(stream)
-        for i in range(K):
-            r = Wm + i
-            ev[i][0].record(stream)
-            verify(r)
-            ev[i][1].record(stream)
-            eng.realign(drafts[r], copy_engine=args.copy_engine)
-            ev[i][2].record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            rounds(not fused)
         t1.record(stream)
         torch.cuda.synchronize()
     barrier(ws)
@@ -336,6 +380,12 @@ def run_specdec(args, rank, ws, local):
     status = int(eng.status.item())
     if status:
         raise RuntimeError(f"device status {status} during the timed rounds")
+    if fused:  # the per-kernel breakdown, from a pass with events
+        eng.pdl = False
+        warm()
+        rounds(True)
+        torch.cuda.synchronize()
+        eng.pdl = use_pdl
     t_verify = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     t_realign = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     n_hist = eng.n_hist.cpu().numpy().astype(np.int64)
@@ -376,9 +426,13 @@ def run_specdec(args, rank, ws, local):
                 eng.verify_greedy(dev_lg, dev_d)
             else:
                 dev_dl.copy_(pin_dl[r], non_blocking=True)
-                dev_u.copy_(pin_u[r], non_blocking=True)
-                eng.verify_sample(dev_lg, dev_dl, dev_d, dev_u, w.temperature,
-                                  top_k=args.top_k, top_p=args.top_p)
+                if args.philox:
+                    eng.verify_sample(dev_lg, dev_dl, dev_d, None, w.temperature,
+                                      top_k=args.top_k, top_p=args.top_p, seed=w.seed)
+                else:
+                    dev_u.copy_(pin_u[r], non_blocking=True)
+                    eng.verify_sample(dev_lg, dev_dl, dev_d, dev_u, w.temperature,
+                                      top_k=args.top_k, top_p=args.top_p)
             eng.realign(dev_d, copy_engine=args.copy_engine)
             if i is not None:
                 out[i, :w.B].copy_(eng.accept_len, non_blocking=True)
@@ -401,7 +455,8 @@ def run_specdec(args, rank, ws, local):
         barrier(ws)
         e2e_ms = max_over_ranks(s0.elapsed_time(s1), ws)
         h2d = sum(x.numel() * x.element_size() for x in
-                  [pin_lg[0], pin_d[0]] + ([pin_dl[0], pin_u[0]] if pin_dl else []))
+                  [pin_lg[0], pin_d[0]] + ([pin_dl[0]] if pin_dl else [])
+                  + ([pin_u[0]] if pin_dl and not args.philox else []))
         e2e = {"value": K * ws / (e2e_ms / 1e3), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": out[0].numel() * 4}
 
@@ -413,6 +468,7 @@ def run_specdec(args, rank, ws, local):
     return {
         "value": rounds_all / (ms_max / 1e3),
         "ms_per_step": ms_max / K,
+        "launch": launch_used,
         "clocks": clk.summary(),
         "e2e": e2e,
         "roofline": {"bound": "hbm", "kernel": "realign", "achieved": round(achieved, 1),
@@ -796,7 +852,8 @@ def main():
               **({"top_k": args.top_k, "top_p": args.top_p} if filtered else {}),
               "l2": "inputs larger than L2: every round streams >= 1 GB of K/V; all rounds' "
                     "score rows are distinct and generated before the timed region",
-              "parallelism": f"replicas x{ws}"}
+              "parallelism": f"replicas x{ws}",
+              "launch": args.launch}
     line = {"metric": METRIC, "unit": "rounds/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config}
@@ -857,6 +914,9 @@ def main():
                     gpu_launches=(3 if filtered else 2) * args.steps,
                     cpu_baseline=cpu)
         line["config"]["cap_cols"] = res["cap_cols"]
+        line["config"]["launch"] = res["launch"]
+        if args.philox and w.mode == "sampled":
+            line["config"]["uniforms"] = "in-kernel Philox4x32-10"
         line["config"]["kv_buffers"] = 2 if args.ping_pong else 1
         print(json.dumps(line))
 

@@ -165,6 +165,29 @@ int specdec_verify_sample(const void* target_logits, const void* draft_logits, i
                           int32_t* dev_status, void* stream);
 
 /*
+ * Sampled verification with the uniforms drawn in-kernel (the fused round needs no uniform
+ * buffer).  [Counter-based generator: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
+ * Easy as 1, 2, 3" (SC11), Philox4x32-10.]  As specdec_verify_sample, with u[b][j] (j = 0..D)
+ * = (x >> 8) * 2^-24, where x is word j mod 4 of Philox4x32-10 at counter
+ * (j div 4, b, offset mod 2^32, offset div 2^32) and key (seed mod 2^32, seed div 2^32): 24-bit
+ * uniforms in [0, 1), the same in fp32 and fp64.  The caller advances `offset` every round (any
+ * (seed, offset) pair gives an independent stream of B * 8 blocks).
+ */
+int specdec_verify_sample_philox(const void* target_logits, const void* draft_logits, int dtype,
+                                 int B, int D, int V, long long row_stride, float temperature,
+                                 const int32_t* draft, uint64_t seed, uint64_t offset,
+                                 int32_t* accept_len, int32_t* out_token, float* residual_out,
+                                 const void* keep_bounds, int32_t* dev_status, void* stream);
+
+/*
+ * The uniforms u[B][D+1] (fp32, row-major, device memory) that specdec_verify_sample_philox draws
+ * for (seed, offset): to log or replay a round through specdec_verify_sample.  Limits: B >= 0,
+ * 1 <= D <= 31.
+ */
+int specdec_philox_uniforms(uint64_t seed, uint64_t offset, int B, int D, float* out,
+                            void* stream);
+
+/*
  * The kept set of one score row under the sampling settings, as its last token in the settings'
  * order.  A token with score x at index v is kept iff key(x) > key, or key(x) == key and
  * v <= index, where key(x) is the order-preserving code of the score as a float: its IEEE bits
@@ -260,7 +283,17 @@ typedef struct {
   int32_t* n_committed_dst;       /* [B]  N'_b */
   int32_t* width_dst;             /* [1]  W' */
   int32_t* dev_status;            /* [1] */
+  int flags;                      /* 0, or SPECDEC_REALIGN_PDL */
 } specdec_realign_args;
+
+/*
+ * SPECDEC_REALIGN_PDL: launch the realignment with programmatic stream serialization, so that it
+ * may be launched while the kernel ahead of it on the stream (normally the verification, which
+ * signals its dependents as it starts) is still running; the realignment waits for that kernel to
+ * complete, and for its writes to be visible, before it reads or writes anything.  The result is
+ * the same; the launch latency between the two kernels is hidden.
+ */
+#define SPECDEC_REALIGN_PDL 1
 
 int specdec_realign(const specdec_realign_args* args, void* stream);
 

@@ -43,6 +43,16 @@ template <> struct Vec<float> {
   __device__ __forceinline__ static float scalar(const float* p) { return *p; }
 };
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialization may
+// start before the kernel ahead of it on the stream has finished; pdl_wait() blocks until that
+// kernel has completed and its memory operations are visible (a no-op for a normal launch).
+// pdl_launch_dependents() lets the next such kernel start launching once every CTA of this grid
+// has called it or exited (without it, that happens when this grid completes).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Streaming 16-byte load that does not allocate in L1 (each byte is read once).
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 r;

@@ -61,6 +61,7 @@ struct Params {
   ByteView src, dst;
   int mode, R, D, L, H, col_bytes, tile, stages, copy_engine, in_place, by_slot;
   int kv_in_place;  // EQSPEC: src and dst are one K/V buffer
+  int pdl;          // launch with programmatic stream serialization
   int32_t pad_id;
   // EQSPEC
   const int32_t* n_committed;
@@ -442,6 +443,9 @@ __device__ void write_metadata(const Params& p, const Plan& s, long long gt, lon
 }
 
 __global__ void __launch_bounds__(kThreads) realign_kernel(const Params p) {
+  // Launched with programmatic serialization, this grid may be resident before the verification
+  // ahead of it has finished: wait for it before reading anything it wrote.
+  pdl_wait();
   extern __shared__ __align__(128) char dyn[];
   __shared__ Plan s;
   __shared__ int red[72];
@@ -547,6 +551,19 @@ int launch(Params& p, cudaStream_t stream) {
     attr_set[dev] = true;
   }
   const int grid = sms * SPECDEC_REALIGN_CTAS_PER_SM;
+  if (p.pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return map_cuda_error(cudaLaunchKernelEx(&cfg, realign_kernel, p));
+  }
   realign_kernel<<<grid, kThreads, smem, stream>>>(p);
   return map_cuda_error(cudaGetLastError());
 }
@@ -621,6 +638,7 @@ int realign_common(const specdec_realign_args* a, bool in_place, void* stream) {
   if (a->B < 0 || a->D < 1) return SPECDEC_ERR_INVALID_ARG;
   if (a->D > SPECDEC_MAX_DRAFT || a->B > kMaxRows) return SPECDEC_ERR_UNSUPPORTED;
   if (a->copy_engine != 0 && a->copy_engine != 1) return SPECDEC_ERR_INVALID_ARG;
+  if (a->flags & ~SPECDEC_REALIGN_PDL) return SPECDEC_ERR_INVALID_ARG;
   if (a->B == 0) return SPECDEC_OK;
   int st = check_view(a->src, 0);
   if (st) return st;
@@ -674,6 +692,7 @@ int realign_common(const specdec_realign_args* a, bool in_place, void* stream) {
   p.width_dst = a->width_dst;
   p.status = a->dev_status;
   p.kv_in_place = in_place ? 1 : 0;
+  p.pdl = (a->flags & SPECDEC_REALIGN_PDL) ? 1 : 0;
   return launch(p, static_cast<cudaStream_t>(stream));
 }
 

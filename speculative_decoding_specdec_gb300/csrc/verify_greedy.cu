@@ -190,6 +190,7 @@ template <typename T, bool kVec>
 __global__ void __launch_bounds__(kThreads, 2) greedy_kernel(const GreedyArgs A) {
   __shared__ unsigned long long s_key[kMaxSegs];
   __shared__ unsigned char s_last[kMaxSegs];
+  pdl_launch_dependents();  // a realignment launched after this may start its launch now
 
   constexpr int VN = kVec ? Vec<T>::N : 1;
   const int c = blockIdx.x;
@@ -285,6 +286,7 @@ constexpr int kRingChunkUnits = kRingChunk / 16;
 
 template <typename T>
 __global__ void __launch_bounds__(kRingThreads, 1) greedy_ring_kernel(const GreedyArgs A) {
+  pdl_launch_dependents();  // a realignment launched after this may start its launch now
   extern __shared__ __align__(128) char ring[];
   __shared__ unsigned long long s_key[kMaxSegs];
   __shared__ unsigned char s_last[kMaxSegs];

@@ -233,7 +233,40 @@ struct SampleArgs {
   float* residual;
   const uint2* keep;  // [B][2D+1] keep bounds of the sampling settings, or NULL (keep all)
   int32_t* status;
+  unsigned long long seed, offset;  // uniforms == NULL: drawn in-kernel (philox_uniform)
 };
+
+// Philox4x32-10 ("Parallel Random Numbers: As Easy as 1, 2, 3", SC11): ten rounds of
+// (hi0, lo0) = M0 * c0, (hi1, lo1) = M1 * c2, c = (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0), with
+// the key advanced by the Weyl increments between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+  constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+  constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k.x += kW0;
+      k.y += kW1;
+    }
+    const uint32_t hi0 = __umulhi(kM0, c.x), lo0 = kM0 * c.x;
+    const uint32_t hi1 = __umulhi(kM1, c.z), lo1 = kM1 * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+  }
+  return c;
+}
+
+// The uniform u[b][j] of a round drawn from (seed, offset): word j mod 4 of Philox4x32-10 at
+// counter (j div 4, b, offset lo, offset hi) and key (seed lo, seed hi), as a 24-bit value in
+// [0, 1) (exact in fp32).
+__device__ __forceinline__ float philox_uniform(unsigned long long seed, unsigned long long offset,
+                                                int b, int j) {
+  const uint4 x = philox4x32_10(
+      make_uint4(static_cast<uint32_t>(j >> 2), static_cast<uint32_t>(b),
+                 static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32)),
+      make_uint2(static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)));
+  const uint32_t w = (j & 3) == 0 ? x.x : (j & 3) == 1 ? x.y : (j & 3) == 2 ? x.z : x.w;
+  return static_cast<float>(w >> 8) * (1.0f / 16777216.0f);
+}
 
 // A row's keep bound (order-preserving 32-bit key of the last kept score, its index) as a float
 // threshold: a token with score x at index v is kept iff x > t, or x == t and v <= ti.  Keys at
@@ -260,6 +293,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
   constexpr int kThreads = Cfg<W>::kThreads, kConsumers = Cfg<W>::kConsumers;
   constexpr int kRingBytes = Cfg<W>::kRingBytes;
   extern __shared__ __align__(128) char dyn[];  // phase 1: the ring; phase 3: two staged rows
+  pdl_launch_dependents();  // a realignment launched after this may start its launch now
   __shared__ float po[kMaxQ][kWarps];
   __shared__ float ps[kMaxQ][kWarps];
   __shared__ float co[kMaxQ];   // this CTA's per-row partials, read by the whole cluster
@@ -307,7 +341,9 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
   // Draft tokens, uniforms and the two scores of each draft: fetched by the producer warp's idle
   // lanes 1..31 while the slice streams (item j = lane - 1, lane + 30, ...; D+1 uniforms).
   auto prefetch = [&](int j) {
-    if (j <= D) pre_u[j] = A.uniforms[static_cast<long long>(b) * (D + 1) + j];
+    if (j <= D)
+      pre_u[j] = A.uniforms ? A.uniforms[static_cast<long long>(b) * (D + 1) + j]
+                            : philox_uniform(A.seed, A.offset, b, j);
     if (j < D) {
       const int d = A.draft[static_cast<long long>(b) * D + j];
       pre_d[j] = d;
@@ -822,20 +858,31 @@ int launch(SampleArgs A, int B, cudaStream_t stream) {
 }  // namespace
 }  // namespace specdec
 
-extern "C" int specdec_verify_sample(const void* target_logits, const void* draft_logits,
-                                     int dtype, int B, int D, int V, long long row_stride,
-                                     float temperature, const int32_t* draft,
-                                     const float* uniforms, int32_t* accept_len,
-                                     int32_t* out_token, float* residual_out,
-                                     const void* keep_bounds, int32_t* dev_status, void* stream) {
-  using namespace specdec;
+namespace specdec {
+namespace {
+
+__global__ void __launch_bounds__(256) philox_uniforms_kernel(unsigned long long seed,
+                                                              unsigned long long offset, int B,
+                                                              int D, float* out) {
+  const long long n = static_cast<long long>(B) * (D + 1);
+  for (long long i = blockIdx.x * 256LL + threadIdx.x; i < n; i += gridDim.x * 256LL)
+    out[i] = philox_uniform(seed, offset, static_cast<int>(i / (D + 1)), static_cast<int>(i % (D + 1)));
+}
+
+int verify_sample_common(const void* target_logits, const void* draft_logits, int dtype, int B,
+                         int D, int V, long long row_stride, float temperature,
+                         const int32_t* draft, const float* uniforms, bool philox,
+                         unsigned long long seed, unsigned long long offset,
+                         int32_t* accept_len, int32_t* out_token,
+                         float* residual_out, const void* keep_bounds, int32_t* dev_status,
+                         void* stream) {
   const int es = elem_size(dtype);
   if (es == 0 || B < 0 || D < 1 || V < 1 || row_stride < V) return SPECDEC_ERR_INVALID_ARG;
   if (!(temperature > 0.f) || !std::isfinite(temperature)) return SPECDEC_ERR_INVALID_ARG;
   if (D > SPECDEC_MAX_DRAFT) return SPECDEC_ERR_UNSUPPORTED;
   if (B == 0) return SPECDEC_OK;
-  if (!target_logits || !draft_logits || !draft || !uniforms || !accept_len || !out_token ||
-      !dev_status)
+  if (!target_logits || !draft_logits || !draft || !accept_len || !out_token || !dev_status ||
+      (!philox && !uniforms))
     return SPECDEC_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(target_logits) % es ||
       reinterpret_cast<uintptr_t>(draft_logits) % es)
@@ -848,9 +895,49 @@ extern "C" int specdec_verify_sample(const void* target_logits, const void* draf
   if (reinterpret_cast<uintptr_t>(keep_bounds) % 8) return SPECDEC_ERR_INVALID_ARG;
   SampleArgs A = {target_logits, draft_logits, D, V, row_stride, temperature, 1, V, draft,
                   uniforms, accept_len, out_token, residual_out,
-                  static_cast<const uint2*>(keep_bounds), dev_status};
+                  static_cast<const uint2*>(keep_bounds), dev_status, seed, offset};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SPECDEC_BF16)
     return vec ? launch<uint16_t, true>(A, B, s) : launch<uint16_t, false>(A, B, s);
   return vec ? launch<float, true>(A, B, s) : launch<float, false>(A, B, s);
+}
+
+}  // namespace
+}  // namespace specdec
+
+extern "C" int specdec_verify_sample(const void* target_logits, const void* draft_logits,
+                                     int dtype, int B, int D, int V, long long row_stride,
+                                     float temperature, const int32_t* draft,
+                                     const float* uniforms, int32_t* accept_len,
+                                     int32_t* out_token, float* residual_out,
+                                     const void* keep_bounds, int32_t* dev_status, void* stream) {
+  return specdec::verify_sample_common(target_logits, draft_logits, dtype, B, D, V, row_stride,
+                                       temperature, draft, uniforms, false, 0ull, 0ull, accept_len,
+                                       out_token, residual_out, keep_bounds, dev_status, stream);
+}
+
+extern "C" int specdec_verify_sample_philox(const void* target_logits, const void* draft_logits,
+                                            int dtype, int B, int D, int V, long long row_stride,
+                                            float temperature, const int32_t* draft,
+                                            uint64_t seed, uint64_t offset, int32_t* accept_len,
+                                            int32_t* out_token, float* residual_out,
+                                            const void* keep_bounds, int32_t* dev_status,
+                                            void* stream) {
+  return specdec::verify_sample_common(target_logits, draft_logits, dtype, B, D, V, row_stride,
+                                       temperature, draft, nullptr, true, seed, offset, accept_len,
+                                       out_token, residual_out, keep_bounds, dev_status, stream);
+}
+
+extern "C" int specdec_philox_uniforms(uint64_t seed, uint64_t offset, int B, int D, float* out,
+                                       void* stream) {
+  using namespace specdec;
+  if (B < 0 || D < 1) return SPECDEC_ERR_INVALID_ARG;
+  if (D > SPECDEC_MAX_DRAFT || B > (1 << 26)) return SPECDEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPECDEC_OK;
+  if (!out) return SPECDEC_ERR_INVALID_ARG;
+  const long long n = static_cast<long long>(B) * (D + 1);
+  const int grid = static_cast<int>(std::min<long long>((n + 255) / 256, 4096));
+  philox_uniforms_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(seed, offset, B, D,
+                                                                               out);
+  return map_cuda_error(cudaGetLastError());
 }

@@ -48,12 +48,13 @@ class EqspecBatch:
     ids, mask and positions stay double-buffered."""
 
     def __init__(self, layers, heads, head_dim, kv_dtype, B, D, cap, max_rounds, device="cuda",
-                 pad_id=0, in_place=False):
+                 pad_id=0, in_place=False, pdl=False):
         self.L, self.H, self.hd, self.B, self.D, self.cap = layers, heads, head_dim, B, D, cap
         self.max_rounds = max_rounds
         self.pad_id = pad_id
         dev = torch.device(device)
         self.in_place = in_place
+        self.pdl = pdl
         self.kv = [torch.empty((layers, 2, B, heads, cap, head_dim), dtype=kv_dtype, device=dev)
                    for _ in range(1 if in_place else 2)]
         self.ids = [torch.full((B, cap), pad_id, dtype=torch.int32, device=dev) for _ in range(2)]
@@ -114,19 +115,29 @@ class EqspecBatch:
                               self.workspaces.greedy(logits, draft), stream)
 
     def verify_sample(self, target_logits, draft_logits, draft, uniforms, temperature,
-                      residual=None, stream=None, top_k=0, top_p=1.0):
+                      residual=None, stream=None, top_k=0, top_p=1.0, seed=None):
         """Sampled verification; with top_k / top_p the rows' keep bounds are computed first
-        (specdec_sampling_filter) into a buffer this batch keeps."""
+        (specdec_sampling_filter) into a buffer this batch keeps.  ``uniforms`` None: they are
+        drawn in-kernel from ``seed`` with this round's index as the Philox offset."""
         bounds = None
         if (0 < top_k < target_logits.shape[-1]) or top_p < 1.0:
             bounds = self.workspaces.bounds(draft)
             specdec.sampling_filter(target_logits, draft_logits, temperature, top_k, top_p,
                                     bounds, self.status, stream)
+        if uniforms is None:
+            if seed is None:
+                raise ValueError("in-kernel uniforms need a seed")
+            specdec.verify_sample_philox(target_logits, draft_logits, draft, seed, self.round,
+                                         temperature, self.accept_len, self.out_token,
+                                         self.status, residual, stream, keep_bounds=bounds)
+            return
         specdec.verify_sample(target_logits, draft_logits, draft, uniforms, temperature,
                               self.accept_len, self.out_token, self.status, residual, stream,
                               keep_bounds=bounds)
 
     def realign(self, draft, copy_engine=0, stream=None):
+        """Realign after this round's verification; with ``pdl`` (constructor) the realignment
+        is launched as a programmatic dependent of the verification kernel ahead of it."""
         r = self.round
         if r >= self.max_rounds:
             raise RuntimeError("round history is full")
@@ -135,7 +146,7 @@ class EqspecBatch:
         specdec.realign(ks, kd, self.n_hist[r], self.w_hist[r], self.accept_len,
                         self.out_token, draft, self.ids[s], self.ids[d], self.mask[d],
                         self.pos[d], self.n_hist[r + 1], self.w_hist[r + 1], self.status,
-                        pad_id=self.pad_id, copy_engine=copy_engine, stream=stream)
+                        pad_id=self.pad_id, copy_engine=copy_engine, pdl=self.pdl, stream=stream)
         self.cur = d
         self.round = r + 1
 

@@ -22,6 +22,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_CAPACITY, ERR_INPUT_RANGE, E
 F32, BF16 = 0, 1
 MAX_DRAFT = 31
 GREEDY_SCRATCH_BYTES = 73728   # SPECDEC_GREEDY_SCRATCH_BYTES
+REALIGN_PDL = 1                # SPECDEC_REALIGN_PDL
 
 c_i32p = ctypes.POINTER(ctypes.c_int32)
 
@@ -42,7 +43,8 @@ class RealignArgs(ctypes.Structure):
                 ("draft", ctypes.c_void_p), ("ids_src", ctypes.c_void_p),
                 ("ids_dst", ctypes.c_void_p), ("mask_dst", ctypes.c_void_p),
                 ("pos_dst", ctypes.c_void_p), ("n_committed_dst", ctypes.c_void_p),
-                ("width_dst", ctypes.c_void_p), ("dev_status", ctypes.c_void_p)]
+                ("width_dst", ctypes.c_void_p), ("dev_status", ctypes.c_void_p),
+                ("flags", ctypes.c_int)]
 
 
 class PoolArgs(ctypes.Structure):
@@ -109,6 +111,12 @@ if hasattr(lib, "specdec_verify_sample"):
     lib.specdec_verify_sample.restype = _i
     lib.specdec_verify_sample.argtypes = [_vp, _vp, _i, _i, _i, _i, _ll, _f, _vp, _vp, _vp, _vp,
                                           _vp, _vp, _vp, _vp]
+lib.specdec_philox_uniforms.restype = _i
+lib.specdec_philox_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_uint64, _i, _i, _vp, _vp]
+lib.specdec_verify_sample_philox.restype = _i
+lib.specdec_verify_sample_philox.argtypes = [_vp, _vp, _i, _i, _i, _i, _ll, _f, _vp,
+                                             ctypes.c_uint64, ctypes.c_uint64, _vp, _vp, _vp,
+                                             _vp, _vp, _vp]
 lib.specdec_sampling_filter.restype = _i
 lib.specdec_sampling_filter.argtypes = [_vp, _vp, _i, _i, _i, _i, _ll, _f, _i, _f, _vp, _vp, _vp]
 lib.specdec_pool_schedule.restype = _i
@@ -291,18 +299,53 @@ def verify_sample(target_logits, draft_logits, draft, uniforms, temperature, acc
            "specdec_verify_sample")
 
 
+def philox_uniforms(seed, offset, out, stream=None):
+    """The uniforms [B, D+1] that verify_sample_philox draws for (seed, offset), into ``out``."""
+    _need(out, torch.float32, "out")
+    if out.dim() != 2 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [B, D+1] float32 tensor")
+    B, Dp1 = out.shape
+    _check(lib.specdec_philox_uniforms(int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1),
+                                       B, Dp1 - 1, _ptr(out), _stream(stream)),
+           "specdec_philox_uniforms")
+
+
+def verify_sample_philox(target_logits, draft_logits, draft, seed, offset, temperature,
+                         accept_len, out_token, status, residual=None, stream=None,
+                         keep_bounds=None):
+    """Sampled verification with the uniforms drawn in-kernel from (seed, offset) by
+    Philox4x32-10 (see specdec.h); advance ``offset`` every round."""
+    B, D = draft.shape
+    V = target_logits.shape[-1]
+    rs = _score_rows(target_logits, B, D + 1, "target_logits")
+    rs2 = _score_rows(draft_logits, B, D, "draft_logits")
+    if rs != rs2 or draft_logits.dtype != target_logits.dtype or draft_logits.shape[-1] != V:
+        raise ValueError("target and draft scores must share dtype, V and row stride")
+    if residual is not None:
+        _need(residual, torch.float32, "residual")
+        if tuple(residual.shape) != (B, V) or not residual.is_contiguous():
+            raise ValueError("residual must be a contiguous [B, V] float32 tensor")
+    _check(lib.specdec_verify_sample_philox(
+        _ptr(target_logits), _ptr(draft_logits), dtype_code(target_logits.dtype), B, D, V, rs,
+        float(temperature), _ptr(draft), int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1),
+        _ptr(accept_len), _ptr(out_token), _ptr(residual), _ptr(keep_bounds), _ptr(status),
+        _stream(stream)), "specdec_verify_sample_philox")
+
+
 def realign(src, dst, n_committed, width, accept_len, out_token, draft, ids_src, ids_dst,
             mask_dst, pos_dst, n_committed_dst, width_dst, status, pad_id=0, copy_engine=0,
-            stream=None):
+            pdl=False, stream=None):
     """EQSPEC realignment from cache ``src`` into cache ``dst`` (both [L, 2, B, H, cap, hd]).
     Passing the same tensor as ``src`` and ``dst`` moves the K/V in place
-    (specdec_realign_inplace); the metadata outputs stay separate."""
+    (specdec_realign_inplace); the metadata outputs stay separate.  ``pdl`` launches it as a
+    programmatic dependent of the kernel ahead of it (SPECDEC_REALIGN_PDL)."""
     B, D = draft.shape
     in_place = src.data_ptr() == dst.data_ptr()
     a = RealignArgs()
     a.src = kv_view(src)
     a.dst = kv_view(dst)
     a.B, a.D, a.pad_id, a.copy_engine = B, D, int(pad_id), int(copy_engine)
+    a.flags = REALIGN_PDL if pdl else 0
     for name, t in (("n_committed", n_committed), ("width", width), ("accept_len", accept_len),
                     ("out_token", out_token), ("draft", draft), ("ids_src", ids_src),
                     ("ids_dst", ids_dst), ("pos_dst", pos_dst),

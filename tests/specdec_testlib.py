@@ -13,7 +13,7 @@ def host_bits(t):
 
 def eqspec_rounds(L, H, hd, kv_dtype, B, D, V, rounds, prompt_lo, prompt_hi, seed,
                   copy_engine=0, alpha=0.6, logit_dtype=torch.float32, cap_extra=0,
-                  check_full_dst=True, in_place=False):
+                  check_full_dst=True, in_place=False, pdl=False):
     """Greedy verify + realign for ``rounds`` rounds with tagged K/V; every round is compared
     with the oracle: accept lengths, tokens, lengths, width, ids, mask, position IDs, and the
     whole destination cache (the oracle leaves pad columns as they were, and so must the
@@ -25,7 +25,7 @@ def eqspec_rounds(L, H, hd, kv_dtype, B, D, V, rounds, prompt_lo, prompt_hi, see
     n0 = synth.lengths_uniform(gen, B, prompt_lo, prompt_hi)
     prompts = [torch.randint(0, V, (int(n),), generator=gen).tolist() for n in n0]
     cap = int(n0.max()) + rounds * (D + 1) + D + 1 + cap_extra
-    eng = EqspecBatch(L, H, hd, kv_dtype, B, D, cap, rounds, in_place=in_place)
+    eng = EqspecBatch(L, H, hd, kv_dtype, B, D, cap, rounds, in_place=in_place, pdl=pdl)
     W = eng.start(prompts)
     eng.kv[0].fill_(-3.0)
     if not in_place:

@@ -22,6 +22,7 @@ def test_every_declared_symbol_is_exported():
     assert "specdec_realign" in names and "specdec_verify_sample" in names
     assert "specdec_verify_greedy_workspace" in names and "specdec_verify_greedy_noalloc" in names
     assert "specdec_pool_schedule" in names and "specdec_arena_destroy" in names
+    assert "specdec_verify_sample_philox" in names and "specdec_philox_uniforms" in names
     missing = [n for n in names if not hasattr(sd.lib, n)]
     assert missing == []
     assert sd.version() == 100
@@ -33,6 +34,7 @@ def test_header_constants_match_binding():
     macro = {m: int(v) for m, v in re.findall(r"^#define (SPECDEC_\w+) (\d+)", text, re.M)}
     assert macro["SPECDEC_MAX_DRAFT"] == sd.MAX_DRAFT
     assert macro["SPECDEC_GREEDY_SCRATCH_BYTES"] == sd.GREEDY_SCRATCH_BYTES
+    assert macro["SPECDEC_REALIGN_PDL"] == sd.REALIGN_PDL
 
 
 def test_status_strings():
@@ -116,6 +118,9 @@ def test_host_validation_codes():
     a.dst = sd.KvView(8192, 64, 32, 16, 8, sd.BF16, 1, 2, 1, 8, 2)
     assert L.specdec_realign_inplace(ctypes.byref(a), None) == sd.ERR_INVALID_ARG
     assert L.specdec_realign_inplace(None, None) == sd.ERR_INVALID_ARG
+    a.flags = 2                                                              # unknown flag
+    assert L.specdec_realign(ctypes.byref(a), None) == sd.ERR_INVALID_ARG
+    a.flags = 0
     # grouping
     assert L.specdec_group_by_length(None, -1, 8, 10, None, None, None, None, None, None, None) == sd.ERR_INVALID_ARG
     assert L.specdec_group_by_length(None, 5000, 8, 10, None, None, None, None, None, None, None) == sd.ERR_UNSUPPORTED
@@ -125,6 +130,15 @@ def test_host_validation_codes():
     assert L.specdec_pool_gather(None, None) == sd.ERR_INVALID_ARG
     p = sd.PoolArgs()
     assert L.specdec_pool_append(ctypes.byref(p), None) == sd.ERR_INVALID_ARG
+    # in-kernel uniforms
+    assert L.specdec_philox_uniforms(1, 2, 0, 3, None, None) == sd.OK                  # nothing to draw
+    assert L.specdec_philox_uniforms(1, 2, 4, 3, None, None) == sd.ERR_INVALID_ARG     # NULL out
+    assert L.specdec_philox_uniforms(1, 2, 4, 0, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_philox_uniforms(1, 2, 4, 32, None, None) == sd.ERR_UNSUPPORTED
+    assert L.specdec_verify_sample_philox(None, None, sd.BF16, 0, 4, 100, 100, 1.0, None, 1, 2,
+                                          None, None, None, None, None, None) == sd.OK
+    assert L.specdec_verify_sample_philox(None, None, sd.BF16, 2, 4, 100, 100, 1.0, None, 1, 2,
+                                          None, None, None, None, None, None) == sd.ERR_INVALID_ARG
     # lifecycle: schedule and admission (host checks; no kernel runs)
     assert L.specdec_pool_schedule(None, None) == sd.ERR_INVALID_ARG
     g = sd.ScheduleArgs()

@@ -214,3 +214,11 @@ def test_full_size_rounds(name, in_place):
         np.testing.assert_array_equal(eng.mask[eng.cur].cpu().numpy(), mask)
         np.testing.assert_array_equal(eng.pos[eng.cur].cpu().numpy(), pos)
         n = n.astype(np.int64)
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+def test_rounds_with_programmatic_dependent_launch(in_place):
+    """Realignment launched as a programmatic dependent of the verification (SPECDEC_REALIGN_PDL)
+    gives the oracle's result in every round."""
+    eqspec_rounds(2, 4, 128, torch.bfloat16, B=8, D=5, V=500, rounds=5, prompt_lo=20,
+                  prompt_hi=300, seed=11, alpha=0.7, in_place=in_place, pdl=True)

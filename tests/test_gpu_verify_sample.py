@@ -364,3 +364,59 @@ def test_keep_bounds_many_equal_scores(ties, top_k, top_p):
             assert O.top_p_margin(rows[0, q].astype(np.float64), 0.7, top_k, top_p) < 2e-6, q
             assert abs(int(got.sum()) - int(exp.sum())) == 1
         assert 0 < got.sum() < ties
+
+
+@pytest.mark.parametrize("seed,offset,B,D", [
+    (0, 0, 3, 4),
+    (2024, 7, 64, 6),
+    (2 ** 64 - 1, 2 ** 40 + 3, 33, 31),        # every bit of seed and offset in use
+    (5, 2 ** 32 - 1, 1, 1),
+])
+def test_philox_uniforms_match_the_oracle(seed, offset, B, D):
+    """The uniforms the fused round draws in-kernel (Philox4x32-10) equal the oracle's, bit for
+    bit (24-bit values are exact in fp32)."""
+    import speculative_decoding_specdec_gb300.specdec as sd
+    out = torch.full((B, D + 1), -1.0, device=DEV)
+    sd.philox_uniforms(seed, offset, out)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy().astype(np.float64),
+                                  O.philox_uniforms(seed, offset, B, D))
+
+
+@pytest.mark.parametrize("B,D,V,dtype,top_k", [
+    (32, 6, 151552, torch.bfloat16, 0),        # GLM-4-9B-shaped
+    (8, 5, 32000, torch.bfloat16, 50),         # with top-k bounds
+    (4, 31, 1000, torch.float32, 0),
+])
+def test_sample_with_in_kernel_uniforms(B, D, V, dtype, top_k):
+    """Uniforms drawn in-kernel give exactly the result of passing the same uniforms explicitly,
+    which matches the oracle."""
+    import speculative_decoding_specdec_gb300.specdec as sd
+    gen = synth.make_gen(5000 + B + D)
+    tl, dl, draft, _ = synth.sampled_round(gen, B, D, V, 0.7, dtype=dtype, draft_candidates=top_k)
+    seed, offset = 99, 3
+    u = torch.empty((B, D + 1), device=DEV)
+    sd.philox_uniforms(seed, offset, u)
+    torch.cuda.synchronize()
+    if top_k:
+        a1, y1, r1, st1 = gpu_sample(tl, dl, draft, u.cpu(), 0.7, top_k=top_k)
+    else:
+        a1, y1 = compare(tl, dl, draft, u.cpu(), 0.7)
+        _, _, r1, st1 = gpu_sample(tl, dl, draft, u.cpu(), 0.7)
+    assert st1 == 0
+    tl_d, dl_d = tl.to(DEV), dl.to(DEV)
+    bounds = None
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    if top_k:
+        bounds = torch.zeros((B, 2 * D + 1, 2), dtype=torch.int32, device=DEV)
+        sd.sampling_filter(tl_d, dl_d, 0.7, top_k, 1.0, bounds, st)
+    a = torch.full((B,), -5, dtype=torch.int32, device=DEV)
+    y = torch.full((B,), -5, dtype=torch.int32, device=DEV)
+    res = torch.full((B, V), -1.0, device=DEV)
+    sd.verify_sample_philox(tl_d, dl_d, draft.to(DEV), seed, offset, 0.7, a, y, st, res,
+                            keep_bounds=bounds)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    np.testing.assert_array_equal(a.cpu().numpy(), a1)
+    np.testing.assert_array_equal(y.cpu().numpy(), y1)
+    np.testing.assert_array_equal(res.cpu().numpy(), r1)
