@@ -155,6 +155,35 @@ class NvmlClocks:
         return {name for name, bit in self.BITS.items() if self.ull.value & bit}
 
 
+def bind_local_cpus(index):
+    """Restrict this process's threads to the CPU cores NVML reports as local to the GPU, so that
+    pinned host buffers (allocated and touched by these threads) land on the GPU's NUMA node.
+    Returns (cores now allowed, whether the set was narrowed); a no-op where NVML cannot say."""
+    import ctypes
+    import torch
+    allowed = os.sched_getaffinity(0)
+    if not torch.cuda.is_available():
+        return len(allowed), False
+    try:
+        uuid = str(torch.cuda.get_device_properties(index).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        nv = NvmlClocks(uuid)
+        if not nv.ok:
+            return len(allowed), False
+        words = (ctypes.c_ulong * 64)()
+        if nv.lib.nvmlDeviceGetCpuAffinity(nv.handle, 64, words) != 0:
+            return len(allowed), False
+    except (AttributeError, RuntimeError, OSError):
+        return len(allowed), False
+    bits = ctypes.sizeof(ctypes.c_ulong) * 8
+    local = {w * bits + b for w in range(64) for b in range(bits) if (words[w] >> b) & 1}
+    keep = local & allowed
+    if not keep or keep == allowed:
+        return len(allowed), False
+    os.sched_setaffinity(0, keep)
+    return len(keep), True
+
+
 class ClockSampler:
     """SM clock and clock-event reasons sampled while the timed region runs: an NVML thread polling
     back to back (timed regions can be a few ms long), else nvidia-smi every 10 ms (started
@@ -409,59 +438,54 @@ def run_specdec(args, rank, ws, local):
     committed = float(sum(int(a.sum()) + len(a) for a in acc)) / K
 
     # ---------------- end to end through the public API with host buffers
+    # HostRounds copies each round's inputs from pinned host memory on a copy stream, overlapping
+    # the round before, and reads each round's results back into pinned host memory.
     e2e = None
     if not args.no_e2e:
-        pin_lg = [x.cpu().pin_memory() for x in logits]
-        pin_d = [x.cpu().pin_memory() for x in drafts]
-        pin_dl = [x.cpu().pin_memory() for x in draft_logits]
-        pin_u = [x.cpu().pin_memory() for x in uniforms]
-        dev_lg = torch.empty_like(logits[0])
-        dev_d = torch.empty_like(drafts[0])
-        dev_dl = torch.empty_like(draft_logits[0]) if draft_logits else None
-        dev_u = torch.empty_like(uniforms[0]) if uniforms else None
-        out = torch.empty((K, 2 * w.B + w.B + 1), dtype=torch.int32).pin_memory()
-        eng.start(prompts)
+        from speculative_decoding_specdec_gb300.engine import HostRounds
+        host = []
+        for r in range(R):
+            h = {"logits": logits[r], "draft": drafts[r]}
+            if w.mode == "sampled":
+                h["draft_logits"] = draft_logits[r]
+                if not args.philox:
+                    h["uniforms"] = uniforms[r]
+            host.append({k: v.cpu().pin_memory() for k, v in h.items()})
+        feed = HostRounds(eng, host[0], stream)
+        out = torch.empty((R, 3 * w.B + 1), dtype=torch.int32).pin_memory()
 
-        def e2e_round(r, i):
-            dev_lg.copy_(pin_lg[r], non_blocking=True)
-            dev_d.copy_(pin_d[r], non_blocking=True)
+        def step(d):
             if w.mode == "greedy":
-                eng.verify_greedy(dev_lg, dev_d)
+                eng.verify_greedy(d["logits"], d["draft"])
+            elif args.philox:
+                eng.verify_sample(d["logits"], d["draft_logits"], d["draft"], None, w.temperature,
+                                  top_k=args.top_k, top_p=args.top_p, seed=w.seed)
             else:
-                dev_dl.copy_(pin_dl[r], non_blocking=True)
-                if args.philox:
-                    eng.verify_sample(dev_lg, dev_dl, dev_d, None, w.temperature,
-                                      top_k=args.top_k, top_p=args.top_p, seed=w.seed)
-                else:
-                    dev_u.copy_(pin_u[r], non_blocking=True)
-                    eng.verify_sample(dev_lg, dev_dl, dev_d, dev_u, w.temperature,
-                                      top_k=args.top_k, top_p=args.top_p)
-            eng.realign(dev_d, copy_engine=args.copy_engine)
-            if i is not None:
-                out[i, :w.B].copy_(eng.accept_len, non_blocking=True)
-                out[i, w.B:2 * w.B].copy_(eng.out_token, non_blocking=True)
-                out[i, 2 * w.B:3 * w.B].copy_(eng.n_committed, non_blocking=True)
-                out[i, 3 * w.B:].copy_(eng.width, non_blocking=True)
+                eng.verify_sample(d["logits"], d["draft_logits"], d["draft"], d["uniforms"],
+                                  w.temperature, top_k=args.top_k, top_p=args.top_p)
 
-        for r in range(Wm):
-            e2e_round(r, None)
+        eng.start(prompts)
+        feed.run(host[:Wm], step, out)
         torch.cuda.synchronize()
         barrier(ws)
         torch.cuda.synchronize()
         s0 = torch.cuda.Event(enable_timing=True)
         s1 = torch.cuda.Event(enable_timing=True)
         s0.record(stream)
-        for i in range(K):
-            e2e_round(Wm + i, i)
+        feed.run(host[Wm:], step, out)
         s1.record(stream)
         torch.cuda.synchronize()
         barrier(ws)
         e2e_ms = max_over_ranks(s0.elapsed_time(s1), ws)
-        h2d = sum(x.numel() * x.element_size() for x in
-                  [pin_lg[0], pin_d[0]] + ([pin_dl[0]] if pin_dl else [])
-                  + ([pin_u[0]] if pin_dl and not args.philox else []))
-        e2e = {"value": K * ws / (e2e_ms / 1e3), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": out[0].numel() * 4}
+        if int(eng.status.item()):
+            raise RuntimeError("device status set during the end-to-end rounds")
+        n_e2e = out[:K, 2 * w.B:3 * w.B].numpy().astype(np.int64)
+        if not (n_e2e == n_hist[Wm + 1:R + 1]).all():
+            raise RuntimeError("end-to-end rounds committed other lengths than the device rounds")
+        e2e = {"value": K * ws / (e2e_ms / 1e3), "unit": "rounds/s",
+               "h2d_bytes_per_step": feed.h2d_bytes, "d2h_bytes_per_step": feed.d2h_bytes,
+               "copies": "H2D on a copy stream overlapping the previous round; D2H after each "
+                         "round"}
 
     ms_max = max_over_ranks(ms, ws)
     rounds_all = sum_over_ranks(float(K), ws)
@@ -904,6 +928,8 @@ def main():
                         higher_is_better=False, **res)
             print(json.dumps(line))
         return
+    cores, narrowed = bind_local_cpus(local if ws > 1 else 0)
+    config["host_cpus"] = f"{cores} cores" + (" local to the GPU (NVML affinity)" if narrowed else "")
     res = run_specdec(args, rank, ws, local)
     if rank == 0:
         cpu = None

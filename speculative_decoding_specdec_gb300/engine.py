@@ -60,10 +60,14 @@ class EqspecBatch:
         self.ids = [torch.full((B, cap), pad_id, dtype=torch.int32, device=dev) for _ in range(2)]
         self.mask = [torch.zeros((B, cap), dtype=torch.uint8, device=dev) for _ in range(2)]
         self.pos = [torch.zeros((B, cap), dtype=torch.int32, device=dev) for _ in range(2)]
-        self.n_hist = torch.zeros((max_rounds + 1, B), dtype=torch.int32, device=dev)
-        self.w_hist = torch.zeros((max_rounds + 1, 1), dtype=torch.int32, device=dev)
-        self.accept_len = torch.zeros(B, dtype=torch.int32, device=dev)
-        self.out_token = torch.zeros(B, dtype=torch.int32, device=dev)
+        # Per-round history, row r = [N (B), W, accept lengths (B), tokens (B)]: N and W at the
+        # start of round r, round r's verification results.  Round r's results and the lengths
+        # and width they produce (row r + 1) are one contiguous span of 3B + 1 ints.
+        self.hist = torch.zeros((max_rounds + 1, 3 * B + 1), dtype=torch.int32, device=dev)
+        self.n_hist = self.hist[:, :B]
+        self.w_hist = self.hist[:, B:B + 1]
+        self.accept_len = self.hist[0, B + 1:2 * B + 1]
+        self.out_token = self.hist[0, 2 * B + 1:]
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.workspaces = Workspaces(dev)
         self.round = 0
@@ -88,6 +92,8 @@ class EqspecBatch:
             mask[b, lo:W] = 1
             pos[b, lo:W] = torch.arange(len(p), dtype=torch.int32)
         self.round, self.cur = 0, 0
+        self.accept_len = self.hist[0, B + 1:2 * B + 1]
+        self.out_token = self.hist[0, 2 * B + 1:]
         self.ids[0].copy_(ids)
         self.mask[0].copy_(mask)
         self.pos[0].copy_(pos)
@@ -110,7 +116,22 @@ class EqspecBatch:
         return self.w_hist[self.round]
 
     # ------------------------------------------------------------------ one round
+    def _results_row(self):
+        """Point accept_len / out_token at this round's row of the history."""
+        r, B = self.round, self.B
+        if r >= self.max_rounds:
+            raise RuntimeError("round history is full")
+        self.accept_len = self.hist[r, B + 1:2 * B + 1]
+        self.out_token = self.hist[r, 2 * B + 1:]
+
+    def results_span(self, r):
+        """Round r's results as one contiguous int32 view [accept lengths (B), tokens (B),
+        committed lengths after the round (B), width after the round]."""
+        n = 3 * self.B + 1
+        return self.hist.view(-1)[r * n + self.B + 1:(r + 1) * n + self.B + 1]
+
     def verify_greedy(self, logits, draft, stream=None):
+        self._results_row()
         specdec.verify_greedy(logits, draft, self.accept_len, self.out_token, self.status,
                               self.workspaces.greedy(logits, draft), stream)
 
@@ -119,6 +140,7 @@ class EqspecBatch:
         """Sampled verification; with top_k / top_p the rows' keep bounds are computed first
         (specdec_sampling_filter) into a buffer this batch keeps.  ``uniforms`` None: they are
         drawn in-kernel from ``seed`` with this round's index as the Philox offset."""
+        self._results_row()
         bounds = None
         if (0 < top_k < target_logits.shape[-1]) or top_p < 1.0:
             bounds = self.workspaces.bounds(draft)
@@ -149,6 +171,76 @@ class EqspecBatch:
                         pad_id=self.pad_id, copy_engine=copy_engine, pdl=self.pdl, stream=stream)
         self.cur = d
         self.round = r + 1
+
+
+class HostRounds:
+    """Rounds of one ``EqspecBatch`` fed from pinned host memory.
+
+    Each round's inputs are pinned host tensors (for instance ``logits`` and ``draft``, plus
+    ``draft_logits`` and ``uniforms`` for sampled rounds).  They are copied into one of two device
+    staging sets on a copy stream while the round before runs on the compute stream, so the
+    transfer of round i + 1 overlaps the verification and realignment of round i; a staging set is
+    refilled only once the realignment that last read it has finished.  After each realignment the
+    round's results (accept lengths, tokens, committed lengths and the width: 3B + 1 int32, one
+    contiguous span of the batch's history) are copied into a row of a pinned host tensor on a
+    third stream, so no round waits for the copy-back of the one before.
+    """
+
+    def __init__(self, batch: EqspecBatch, like: dict, stream=None):
+        dev = batch.status.device
+        self.batch = batch
+        self.stream = stream or torch.cuda.current_stream(dev)
+        self.copy_stream = torch.cuda.Stream(dev)
+        self.slots = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in like.items()}
+                      for _ in range(2)]
+        self.d2h_stream = torch.cuda.Stream(dev)
+        self.copied = [torch.cuda.Event() for _ in range(2)]
+        self.freed = [torch.cuda.Event() for _ in range(2)]
+        self.h2d_bytes = sum(v.numel() * v.element_size() for v in like.values())
+        self.d2h_bytes = (3 * batch.B + 1) * 4
+
+    def _stage(self, k, host, wait_freed):
+        if wait_freed:
+            self.copy_stream.wait_event(self.freed[k])
+        with torch.cuda.stream(self.copy_stream):
+            for name, t in host.items():
+                self.slots[k][name].copy_(t, non_blocking=True)
+        self.copied[k].record(self.copy_stream)
+
+    def run(self, host_rounds, step, out):
+        """Run ``len(host_rounds)`` rounds.  ``host_rounds[i]`` maps input names to pinned host
+        tensors; ``step(inputs)`` launches round i's verification on the batch given the device
+        copies (the realignment, with ``inputs["draft"]``, follows here); ``out`` is a pinned int32
+        tensor [len(host_rounds), 3B + 1].  Asynchronous: synchronise the stream before reading
+        ``out``."""
+        n = len(host_rounds)
+        if n == 0:
+            return
+        B = self.batch.B
+        if out.shape[0] < n or out.shape[1] != 3 * B + 1 or not out.is_pinned():
+            raise ValueError("out must be a pinned int32 tensor [rounds, 3B + 1]")
+        start = torch.cuda.Event()
+        start.record(self.stream)
+        self.copy_stream.wait_event(start)   # no copy starts before the work issued so far
+        self._stage(0, host_rounds[0], False)
+        for i in range(n):
+            if i + 1 < n:
+                self._stage((i + 1) % 2, host_rounds[i + 1], i >= 1)
+            k = i % 2
+            self.stream.wait_event(self.copied[k])
+            inp = self.slots[k]
+            with torch.cuda.stream(self.stream):
+                r = self.batch.round
+                step(inp)
+                self.batch.realign(inp["draft"])
+                self.freed[k].record(self.stream)
+            # The result copy waits for the round on its own stream: the next round's kernels
+            # do not wait for it (each round's results have their own row of the history).
+            self.d2h_stream.wait_event(self.freed[k])
+            with torch.cuda.stream(self.d2h_stream):
+                out[i].copy_(self.batch.results_span(r), non_blocking=True)
+        self.stream.wait_stream(self.copy_stream)
+        self.stream.wait_stream(self.d2h_stream)
 
 
 class ExspecPool:
