@@ -889,6 +889,7 @@ def main():
     if args.impl == "reference":
         res = run_reference(args, rank, ws)
         if rank == 0:
+            config.pop("launch", None)   # the oracle runs on host cores: no launch mode
             line.update(impl="reference", value=res["value"], ms_per_step=1e3 / res["value"],
                         cpu_baseline=res["cpu_baseline"], dtype="f64",
                         e2e={"value": res["value"], "unit": "rounds/s",

@@ -23,8 +23,8 @@
 // Bytes moved = read + write of every surviving column, nothing else.
 //
 // In place (EQSPEC, one K/V buffer): a run moves within its own head row by the row's shift
-// s = dst_col - src_col.  Every run is handled by one CTA (grid shares are rounded down to run
-// starts), which takes its tiles in ascending column order when s < 0 and descending when s > 0;
+// s = dst_col - src_col.  Every run is handled by one CTA (grid shares end at the nearest run
+// boundary), which takes its tiles in ascending column order when s < 0 and descending when s > 0;
 // since a tile is stored only after its own load and every earlier load has landed, no store
 // reaches source bytes that are still to be read.  Rows with s = 0 move nothing.
 #include <climits>
@@ -32,13 +32,13 @@
 #include "common.cuh"
 
 #ifndef SPECDEC_REALIGN_TILE
-#define SPECDEC_REALIGN_TILE 32768
+#define SPECDEC_REALIGN_TILE 65536
 #endif
 #ifndef SPECDEC_REALIGN_STAGES
 #define SPECDEC_REALIGN_STAGES 3
 #endif
 #ifndef SPECDEC_REALIGN_CTAS_PER_SM
-#define SPECDEC_REALIGN_CTAS_PER_SM 2
+#define SPECDEC_REALIGN_CTAS_PER_SM 1
 #endif
 
 namespace specdec {
@@ -271,8 +271,10 @@ __device__ __forceinline__ Tile decode(const Params& p, const Plan& s, long long
   return tl;
 }
 
-// The first tile of the run that holds tile t (t == total: total).
-__device__ long long run_start(const Params& p, const Plan& s, long long t, long long total) {
+// The run boundary nearest to tile t: the first tile of the run that holds t, or the first tile
+// after that run, whichever is closer (t == total: total).  Monotone in t, so boundaries taken
+// from increasing t still partition the tiles.
+__device__ long long run_boundary(const Params& p, const Plan& s, long long t, long long total) {
   if (t >= total) return total;
   const int per = s.per_group;
   const long long g = t / per;
@@ -282,8 +284,9 @@ __device__ long long run_start(const Params& p, const Plan& s, long long t, long
     const int mid = (lo + hi + 1) >> 1;
     if (s.prefix[mid] <= in) lo = mid; else hi = mid - 1;
   }
-  const int within = in - s.prefix[lo];
-  return t - within % s.tiles[lo];
+  const int c = s.tiles[lo];
+  const int chunk = (in - s.prefix[lo]) % c;
+  return 2 * chunk > c ? t - chunk + c : t - chunk;
 }
 
 // One elected thread moves tiles [t0, t1) through `stages` shared-memory buffers.
@@ -472,9 +475,9 @@ __global__ void __launch_bounds__(kThreads) realign_kernel(const Params p) {
   const long long G = gridDim.x;
   long long t0 = total * blockIdx.x / G;
   long long t1 = total * (blockIdx.x + 1) / G;
-  if (p.kv_in_place) {  // whole runs per CTA: round both ends down to the start of their run
-    t0 = run_start(p, s, t0, total);
-    t1 = run_start(p, s, t1, total);
+  if (p.kv_in_place) {  // whole runs per CTA: move both ends to the nearest run boundary
+    t0 = run_boundary(p, s, t0, total);
+    t1 = run_boundary(p, s, t1, total);
   }
 
   if (p.copy_engine == 0) {
@@ -531,11 +534,13 @@ int launch(Params& p, cudaStream_t stream) {
   const int sms = sm_count();
   if (sms <= 0) return SPECDEC_ERR_CUDA;
   static_assert(SPECDEC_REALIGN_TILE % 16 == 0, "tile must be a multiple of 16 bytes");
-  // The vector engine loads a whole tile before storing it (in place, its destination may
-  // overlap its source): one pass of kThreads * kVecUnroll vectors must cover a tile.
-  static_assert(SPECDEC_REALIGN_TILE <= kThreads * kVecUnroll * 16, "tile larger than one pass");
+  static_assert(SPECDEC_REALIGN_TILE < (1 << 20), "a tile must fit one mbarrier transaction count");
   static_assert(SPECDEC_REALIGN_STAGES >= 2 && SPECDEC_REALIGN_STAGES <= kMaxStages, "stages");
-  p.tile = SPECDEC_REALIGN_TILE;
+  // The vector engine loads a whole tile before storing it (in place, its destination may
+  // overlap its source): its tiles are one pass of kThreads * kVecUnroll vectors at most.
+  constexpr int kVecTile = SPECDEC_REALIGN_TILE < kThreads * kVecUnroll * 16
+                               ? SPECDEC_REALIGN_TILE : kThreads * kVecUnroll * 16;
+  p.tile = p.copy_engine == 0 ? SPECDEC_REALIGN_TILE : kVecTile;
   p.stages = SPECDEC_REALIGN_STAGES;
   const size_t ring = p.copy_engine == 0 ? static_cast<size_t>(p.tile) * p.stages : 0;
   const size_t smem = ring + plan_bytes(p.R);
