@@ -40,6 +40,9 @@
 #ifndef SPECDEC_REALIGN_CTAS_PER_SM
 #define SPECDEC_REALIGN_CTAS_PER_SM 1
 #endif
+#ifndef SPECDEC_APPEND_CTAS_PER_SM
+#define SPECDEC_APPEND_CTAS_PER_SM 4
+#endif
 
 namespace specdec {
 namespace {
@@ -542,6 +545,14 @@ int launch(Params& p, cudaStream_t stream) {
                                ? SPECDEC_REALIGN_TILE : kThreads * kVecUnroll * 16;
   p.tile = p.copy_engine == 0 ? SPECDEC_REALIGN_TILE : kVecTile;
   p.stages = SPECDEC_REALIGN_STAGES;
+  int ctas_per_sm = SPECDEC_REALIGN_CTAS_PER_SM;
+  if (p.mode == kPoolAppend && p.copy_engine == 0) {
+    // An append moves at most D + 1 columns per run: one small tile per run, and more CTAs per
+    // SM issuing copies (the number of copies in flight, not their size, bounds these launches).
+    const long long run = static_cast<long long>(p.D + 1) * p.col_bytes;  // a multiple of 16
+    if (run < p.tile) p.tile = static_cast<int>(run);
+    ctas_per_sm = SPECDEC_APPEND_CTAS_PER_SM;
+  }
   const size_t ring = p.copy_engine == 0 ? static_cast<size_t>(p.tile) * p.stages : 0;
   const size_t smem = ring + plan_bytes(p.R);
   constexpr size_t kMaxSmem =
@@ -555,7 +566,7 @@ int launch(Params& p, cudaStream_t stream) {
     if (e != cudaSuccess) return map_cuda_error(e);
     attr_set[dev] = true;
   }
-  const int grid = sms * SPECDEC_REALIGN_CTAS_PER_SM;
+  const int grid = sms * ctas_per_sm;
   if (p.pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

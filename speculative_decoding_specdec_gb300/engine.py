@@ -217,7 +217,8 @@ class HostRounds:
         if n == 0:
             return
         B = self.batch.B
-        if out.shape[0] < n or out.shape[1] != 3 * B + 1 or not out.is_pinned():
+        if (out.dtype != torch.int32 or out.dim() != 2 or out.shape[0] < n
+                or out.shape[1] != 3 * B + 1 or not out.is_pinned()):
             raise ValueError("out must be a pinned int32 tensor [rounds, 3B + 1]")
         start = torch.cuda.Event()
         start.record(self.stream)

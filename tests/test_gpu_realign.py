@@ -25,9 +25,10 @@ def test_tiny_fp32(copy_engine):
 
 @pytest.mark.parametrize("copy_engine", [0, 1])
 def test_multi_tile_ragged_bf16(copy_engine):
-    # runs of up to ~330 columns x 256 B span several 32 KB tiles with a ragged last tile
+    # runs of up to ~730 columns x 256 B span several tiles (64 KB bulk, 32 KB vector) with a
+    # ragged last tile
     eqspec_rounds(2, 4, 128, torch.bfloat16, B=8, D=5, V=500, rounds=4, prompt_lo=20,
-                  prompt_hi=300, seed=1, copy_engine=copy_engine, alpha=0.7)
+                  prompt_hi=700, seed=1, copy_engine=copy_engine, alpha=0.7)
 
 
 @pytest.mark.parametrize("B,D,lo,hi,hd,dtype", [
@@ -45,6 +46,7 @@ def test_shapes(B, D, lo, hi, hd, dtype):
 @pytest.mark.parametrize("B,D,lo,hi,hd,dtype,L,H", [
     (2, 4, 5, 20, 64, torch.float32, 1, 2),      # tiny
     (8, 5, 20, 300, 128, torch.bfloat16, 2, 4),  # multi-tile runs, ragged last tiles
+    (4, 5, 300, 1300, 128, torch.bfloat16, 1, 2),  # runs of 2-6 tiles of 64 KB
     (64, 3, 1, 12, 64, torch.bfloat16, 2, 2),    # many short rows: zero-shift and one-column runs
     (3, 31, 2, 100, 8, torch.bfloat16, 2, 2),    # D = 31, 16-byte columns
     (300, 2, 1, 6, 64, torch.float32, 2, 2),     # more rows than one CTA's threads
@@ -56,10 +58,11 @@ def test_in_place(B, D, lo, hi, hd, dtype, L, H):
                   seed=50 + B + D, alpha=0.6, in_place=True)
 
 
-def test_in_place_long_shifts():
-    # prompts of very different lengths: shifts of hundreds of columns both ways over rounds
+@pytest.mark.parametrize("copy_engine", [0, 1])
+def test_in_place_long_shifts(copy_engine):
+    # prompts of very different lengths: runs of up to ~730 columns shifting both ways
     eqspec_rounds(2, 2, 128, torch.bfloat16, B=6, D=6, V=200, rounds=5, prompt_lo=1,
-                  prompt_hi=700, seed=77, alpha=0.9, in_place=True)
+                  prompt_hi=700, seed=77, alpha=0.9, in_place=True, copy_engine=copy_engine)
 
 
 def test_in_place_rejects_a_different_destination():
