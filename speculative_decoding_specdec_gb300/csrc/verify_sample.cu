@@ -13,7 +13,7 @@
 // SM), whichever lets the B clusters keep more SMs busy (clusters stay inside one GPC, so the
 // usable cluster sizes differ between the two).
 //  Phase 1  a producer thread streams the slice of the 2D+1 score rows (D+1 target, D draft)
-//           through a 192 KB shared-memory ring in 32 KB cp.async.bulk copies (rows stored back
+//           through a 192 KB shared-memory ring in 64 KB cp.async.bulk copies (rows stored back
 //           to back are read as one contiguous range per CTA; its idle lanes meanwhile fetch
 //           the drafts, uniforms and the two scores of every draft); 16 consumer warps keep,
 //           per thread and row, a sum s of 2^(x*c2 - o) with c2 = log2(e)/T and an INTEGER offset
@@ -49,10 +49,10 @@ struct Cfg {
   static constexpr int kAllWarps = W + 1;         // plus the producer warp
   static constexpr int kThreads = kAllWarps * 32;
   static constexpr int kConsumers = W * 32;
-  static constexpr int kRingBytes = W * 12288;    // W/16 * 192 KB: 32 KB stages
+  static constexpr int kRingBytes = W * 12288;    // W/16 * 192 KB
+  static constexpr int kChunkBytes = W * 4096;    // bytes per bulk copy: three ring stages
   static constexpr int kPerSm = 16 / W;           // CTAs per SM
 };
-constexpr int kChunkBytes = 32768;      // bytes per bulk copy
 constexpr int kMaxQ = 2 * SPECDEC_MAX_DRAFT + 1;  // score rows per batch row
 constexpr float kLog2e = 1.4426950408889634f;     // log2(e)
 constexpr float kNegInf = -INFINITY;
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
         plan.blk[plan.nblk++] =
             StreamBlock{reinterpret_cast<const char*>(row_ptr(q) + s0), body, q, s0};
     }
-    plan.finish(kChunkBytes / static_cast<int>(sizeof(T)), kRingBytes);
+    plan.finish(Cfg<W>::kChunkBytes / static_cast<int>(sizeof(T)), kRingBytes);
   }
   __syncthreads();
 
