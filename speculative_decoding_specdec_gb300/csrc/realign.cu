@@ -333,9 +333,19 @@ __device__ void copy_bulk(const Params& p, const Plan& s, long long t0, long lon
   bulk_wait_all();
 }
 
-// All threads of the CTA move tiles [t0, t1) with 16-byte loads/stores.  In place, no byte this
-// kernel writes is read afterwards (tiles go in the shift's direction), so the read-only path
-// stays valid.
+// A coherent 16-byte global load.  In place the kernel writes bytes that other threads of the
+// CTA load, so the non-coherent read-only path is not allowed there: its loads are outside the
+// memory model, and a block barrier does not keep another thread's later store from reaching a
+// load still in flight.  A plain load is ordered before the stores behind the barrier.
+__device__ __forceinline__ uint4 ldg_coherent(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p) : "memory");
+  return r;
+}
+
+// All threads of the CTA move tiles [t0, t1) with 16-byte loads/stores (streaming read-only
+// loads out of place, coherent loads in place).
 __device__ void copy_vec(const Params& p, const Plan& s, long long t0, long long t1) {
   for (long long t = t0; t < t1; ++t) {
     const Tile tl = decode(p, s, t);
@@ -347,7 +357,7 @@ __device__ void copy_vec(const Params& p, const Plan& s, long long t0, long long
 #pragma unroll
       for (int k = 0; k < kVecUnroll; ++k) {
         const int v = base + k * kThreads + threadIdx.x;
-        if (v < nv) buf[k] = ldg_stream(src + v);
+        if (v < nv) buf[k] = p.kv_in_place ? ldg_coherent(src + v) : ldg_stream(src + v);
       }
       // In place a tile's destination may overlap its own source: every thread has loaded its
       // part (tiles are at most kThreads * kVecUnroll vectors) before any thread stores.
