@@ -428,15 +428,24 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
             const int nv = n / VN;
             int v = tid;
             if (filter) {  // sampling settings: tokens outside the row's kept set weigh 0
+              // Four vectors whose largest score is below the keep threshold hold no kept token
+              // and are skipped whole (a NaN is never below it, so it still reaches the fold).
               const KeepF kf = s_keep[q];
               for (; v + 3 * kConsumers < nv; v += 4 * kConsumers) {
                 uint4 r[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) r[k] = v4[v + k * kConsumers];
                 float x[4][VN];
+                float m = kNegInf;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                   Vec<T>::unpack(r[k], x[k]);
+#pragma unroll
+                  for (int i = 0; i < VN; ++i) m = (x[k][i] > m || x[k][i] != x[k][i]) ? x[k][i] : m;
+                }
+                if (m < kf.t) continue;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
                   const int e0 = v0 + (v + k * kConsumers) * VN;
 #pragma unroll
                   for (int i = 0; i < VN; ++i) x[k][i] = masked(kf, x[k][i], e0 + i);
