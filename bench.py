@@ -57,6 +57,9 @@ def parse():
     p.add_argument("--ping-pong", action="store_true",
                    help="two K/V caches, realigned from one into the other (default: one cache "
                         "realigned in place)")
+    p.add_argument("--realign-schedule", default="counter", choices=["counter", "fixed"],
+                   help="realignment work distribution: CTAs take work items from a counter "
+                        "(default), or every CTA moves one fixed share")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--layers", type=int, default=0,
                    help="override the workload's layer count (smaller cache, e.g. for ncu)")
@@ -320,7 +323,7 @@ def run_specdec(args, rank, ws, local):
     prompts = [torch.randint(0, w.V, (int(n),), generator=gen_cpu).tolist() for n in n0]
     cap = w.capacity(int(n0.max()), rounds=R)
     eng = EqspecBatch(w.layers, w.heads, w.head_dim, w.kv_dtype, w.B, w.D, cap, R, device=dev,
-                      in_place=not args.ping_pong)
+                      in_place=not args.ping_pong, scheduled=args.realign_schedule == "counter")
     g = torch.Generator(device=dev).manual_seed(w.seed * 7919 + rank)
     for k in eng.kv:
         k.normal_(generator=g)
@@ -554,16 +557,21 @@ def run_pool(args, rank, ws):
 
     def one_round(r, timed):
         n_before = pool.slot_len.cpu().numpy() if timed else None
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)] if timed else None
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if timed else None
         batches = pool.schedule()
         if timed:
+            # the schedule's readback left the device idle: queue the verification behind a
+            # ~0.1 ms device sleep so that its events time the kernel, not the host's launch
+            torch.cuda._sleep(200_000)
             ev[0].record(stream)
         pool.verify_greedy(logits[r], drafts[r])
+        if timed:
+            ev[1].record(stream)
         for off, k, uni in batches:
             pool.gather(off, k, uni)
             pool.append(off, k, uni, drafts[r])
         if timed:
-            ev[1].record(stream)
+            ev[2].record(stream)
             kern.append(ev)
             perm = pool.perm.cpu().numpy()
             n_after = pool.slot_len.cpu().numpy()
@@ -588,12 +596,22 @@ def run_pool(args, rank, ws):
     wall = max_over_ranks(time.perf_counter() - t0, ws)
     if int(pool.status.item()):
         raise RuntimeError(f"device status {int(pool.status.item())}")
-    kern_ms = [e[0].elapsed_time(e[1]) for e in kern]
+    verify_ms = [e[0].elapsed_time(e[1]) for e in kern]
+    kern_ms = [e[1].elapsed_time(e[2]) for e in kern]
     peak, peak_kind = measured_peaks()
     gbs = sum(moved) / (sum(kern_ms) / 1e3) / 1e9
+    # one greedy verification over every slot: scores [S][D+1][V], drafts, two outputs per slot
+    es = torch.tensor([], dtype=w.logit_dtype).element_size()
+    verify_bytes = w.B * (w.D + 1) * w.V * es + w.B * w.D * 4 + w.B * 8
+    t_verify = float(np.mean(verify_ms))
+    verify_gbs = verify_bytes / (t_verify / 1e3) / 1e9
     return {"value": sum_over_ranks(float(K), ws) / wall, "ms_per_step": wall / K * 1e3,
-            "kernel_ms_per_round": float(np.mean(kern_ms)),
+            "kernel_ms_per_round": float(np.mean(kern_ms)) + t_verify,
             "realign_gbs": round(gbs, 1), "realign_frac": round(gbs / peak, 4),
+            "verify": {"kernel": "greedy_kernel", "ms_per_launch": t_verify,
+                       "bytes_per_launch": verify_bytes, "achieved_gbs": round(verify_gbs, 1),
+                       "frac": round(verify_gbs / peak, 4),
+                       "traffic": captured_traffic("greedy_kernel", verify_bytes)},
             "peak": peak, "peak_source": peak_kind,
             "uniform_row_fraction_per_round": [round(x, 3) for x in uniform_frac],
             "mixed_rows_per_round": mixed_rows}
@@ -759,20 +777,27 @@ def run_sweep(args, rank, ws):
         prompts = [torch.randint(0, base.V, (int(n),), generator=gen).tolist() for n in n0]
         cap = int(n0.max()) + R * (base.D + 1) + base.D + 1
         eng = EqspecBatch(base.layers, base.heads, base.head_dim, base.kv_dtype, B, base.D, cap, R,
-                          device=dev, in_place=not args.ping_pong)
+                          device=dev, in_place=not args.ping_pong,
+                          scheduled=args.realign_schedule == "counter")
         g = torch.Generator(device=dev).manual_seed(B)
         rounds = [synth.greedy_round(g, B, base.D, base.V, 0.7, dtype=base.logit_dtype, device=dev)
                   for _ in range(R)]
         eng.start(prompts)
         stream = torch.cuda.current_stream()
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(R)]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(R)]
         for r, (lg, d) in enumerate(rounds):
+            if B == 1:  # nothing moves, so the device idles: keep the host's launch out of the events
+                torch.cuda._sleep(200_000)
+            ev[r][2].record(stream)
             eng.verify_greedy(lg, d)
             ev[r][0].record(stream)
             eng.realign(d)
             ev[r][1].record(stream)
         torch.cuda.synchronize()
         ms = [ev[r][0].elapsed_time(ev[r][1]) for r in range(Wm, R)]
+        vms = [ev[r][2].elapsed_time(ev[r][0]) for r in range(Wm, R)]
+        es = torch.tensor([], dtype=base.logit_dtype).element_size()
+        vbytes = B * (base.D + 1) * base.V * es + B * base.D * 4 + B * 8
         nh = eng.n_hist.cpu().numpy().astype(np.int64)
         wh = eng.w_hist.cpu().numpy().astype(np.int64)[:, 0]
         def moved(r):  # N'_b - 1 columns per row; in place, rows that do not shift move nothing
@@ -787,7 +812,9 @@ def run_sweep(args, rank, ws):
                     "realign_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                     "moved_gb_per_round": round(float(np.mean(alg)) / 1e9, 3),
                     "padded_copy_gb_per_round": round(float(np.mean(padded)) / 1e9, 3),
-                    "mean_width": round(float(np.mean(wh[Wm + 1:R + 1])), 1)})
+                    "mean_width": round(float(np.mean(wh[Wm + 1:R + 1])), 1),
+                    "verify_ms_per_round": round(float(np.mean(vms)), 4),
+                    "verify_frac": round(vbytes / (float(np.mean(vms)) / 1e3) / 1e9 / peak, 4)})
         del eng, rounds
         torch.cuda.empty_cache()
     return {"sweep": out, "peak": peak, "peak_source": peak_kind}
@@ -957,6 +984,7 @@ def main():
         if args.philox and w.mode == "sampled":
             line["config"]["uniforms"] = "in-kernel Philox4x32-10"
         line["config"]["kv_buffers"] = 2 if args.ping_pong else 1
+        line["config"]["realign_schedule"] = args.realign_schedule
         print(json.dumps(line))
 
 

@@ -284,7 +284,19 @@ typedef struct {
   int32_t* width_dst;             /* [1]  W' */
   int32_t* dev_status;            /* [1] */
   int flags;                      /* 0, or SPECDEC_REALIGN_PDL */
+  uint32_t* schedule;             /* NULL, or [2] caller-owned scheduling words (below) */
 } specdec_realign_args;
+
+/*
+ * schedule (optional, device memory, not in the pages: a launch detail).  NULL: every CTA of the
+ * launch moves one fixed, equal, contiguous share of the tiles.  Non-NULL: two uint32 words that
+ * are zero before the first call; the CTAs take work items (a few tiles; whole runs in place)
+ * from a counter in schedule[0] as they free up, so SMs that stream faster take more, and the
+ * last CTA to finish sets both words back to zero -- one pair serves every later call, in a CUDA
+ * graph too.  Calls that may run at the same time (other streams) need their own pair; calls in
+ * order on one stream may share one.  Results are the same either way.  Ignored with
+ * copy_engine 1.  A pointer that is not 4-byte aligned is SPECDEC_ERR_INVALID_ARG.
+ */
 
 /*
  * SPECDEC_REALIGN_PDL: launch the realignment with programmatic stream serialization, so that it

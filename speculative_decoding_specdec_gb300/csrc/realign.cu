@@ -22,6 +22,14 @@
 // stages-1 loads in flight; the other warps meanwhile write the ids, mask and position IDs.
 // Bytes moved = read + write of every surviving column, nothing else.
 //
+// Scheduling.  With a caller-owned schedule (two 32-bit words), the tiles are cut into work
+// items -- a few tiles, or whole runs in place -- and every CTA's elected thread takes the next
+// item from a counter as its ring frees up, keeping one item taken ahead.  Measured on GB300, the
+// SMs of one launch stream at unequal rates (the first CTA of an equal split finishes ~20 %
+// before the last), so a fixed split leaves SMs idle at the end while items from a counter keep
+// them all busy to the last item.  The last CTA to finish sets the words back to zero.  Without
+// a schedule every CTA takes one fixed, contiguous share.
+//
 // In place (EQSPEC, one K/V buffer): a run moves within its own head row by the row's shift
 // s = dst_col - src_col.  Every run is handled by one CTA (grid shares end at the nearest run
 // boundary), which takes its tiles in ascending column order when s < 0 and descending when s > 0;
@@ -96,6 +104,7 @@ struct Params {
   const int32_t* slot_limit;
   int32_t eos_id;
   int32_t* status;
+  unsigned* sched;  // [2] next work item, finished CTAs (zero between calls); null: fixed shares
 };
 
 struct Plan {  // per-row plan, arrays in dynamic shared memory (7 ints per row)
@@ -103,6 +112,7 @@ struct Plan {  // per-row plan, arrays in dynamic shared memory (7 ints per row)
   int* aux;  // EQSPEC: N_b; pool: N_s
   int* acc;  // EQSPEC / append: a
   int W, Wp, per_group;
+  int runs_per_group;  // runs with at least one tile in one (layer, k/v) group
 };
 
 __host__ __device__ constexpr size_t plan_bytes(int rows) {
@@ -221,8 +231,13 @@ __device__ bool build_plan(const Params& p, Plan& s, int* red) {
     const int lane = threadIdx.x;
     const int per = (R + 31) / 32;
     const int r0 = min(R, lane * per), r1 = min(R, r0 + per);
-    int local = 0;
-    for (int r = r0; r < r1; ++r) local += s.tiles[r] * p.H;
+    int local = 0, runs = 0;
+    for (int r = r0; r < r1; ++r) {
+      local += s.tiles[r] * p.H;
+      runs += s.tiles[r] > 0 ? p.H : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) runs += __shfl_xor_sync(0xffffffffu, runs, o);
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -234,7 +249,10 @@ __device__ bool build_plan(const Params& p, Plan& s, int* red) {
       s.prefix[r] = run;
       run += s.tiles[r] * p.H;
     }
-    if (lane == 31) s.per_group = incl;
+    if (lane == 31) {
+      s.per_group = incl;
+      s.runs_per_group = runs;
+    }
   }
   __syncthreads();
   return true;
@@ -292,21 +310,27 @@ __device__ long long run_boundary(const Params& p, const Plan& s, long long t, l
   return 2 * chunk > c ? t - chunk + c : t - chunk;
 }
 
-// One elected thread moves tiles [t0, t1) through `stages` shared-memory buffers.
-__device__ void copy_bulk(const Params& p, const Plan& s, long long t0, long long t1, char* ring,
+// One elected thread moves the tiles that next_tile() hands out, in that order, through
+// `stages` shared-memory buffers: stages - 1 loads stay in flight behind each store.
+template <class NextTile>
+__device__ void copy_bulk(const Params& p, const Plan& s, NextTile&& next_tile, char* ring,
                           uint64_t* bars, char** ring_dst, uint32_t* ring_bytes) {
   const int S = p.stages;
-  const long long n = t1 - t0;
-  const long long pre = n < S ? n : S;
-  for (long long k = 0; k < pre; ++k) {
-    const Tile tl = decode(p, s, t0 + k);
+  long long issued = 0, t = 0;
+  bool more = true;
+  for (int k = 0; k < S; ++k) {
+    if (!next_tile(t)) {
+      more = false;
+      break;
+    }
+    const Tile tl = decode(p, s, t);
     ring_dst[k] = tl.dst;
     ring_bytes[k] = tl.bytes;
     mbar_arrive_expect_tx(&bars[k], tl.bytes);
-    bulk_g2s(ring + k * p.tile, tl.src, tl.bytes, &bars[k]);
+    bulk_g2s(ring + static_cast<long long>(k) * p.tile, tl.src, tl.bytes, &bars[k]);
+    ++issued;
   }
-  long long issued = pre;
-  for (long long i = 0; i < n; ++i) {
+  for (long long i = 0; i < issued; ++i) {
     const int st = static_cast<int>(i % S);
     const uint32_t parity = static_cast<uint32_t>((i / S) & 1);
     if (!mbar_wait_bounded(&bars[st], parity, kWaitTries)) {
@@ -318,11 +342,16 @@ __device__ void copy_bulk(const Params& p, const Plan& s, long long t0, long lon
     }
     bulk_s2g(ring_dst[st], ring + static_cast<long long>(st) * p.tile, ring_bytes[st]);
     bulk_commit();
-    if (i >= 1 && issued < n) {
-      // Refill the stage of tile i-1 with tile i-1+S: its store must have read shared memory.
+    if (i >= 1 && more) {
+      // Refill the stage of tile i-1 (its store must have read shared memory) with tile
+      // number i-1+S.
       bulk_wait_read<1>();
+      if (!next_tile(t)) {
+        more = false;
+        continue;
+      }
       const int rs = static_cast<int>((i - 1) % S);
-      const Tile tl = decode(p, s, t0 + issued);
+      const Tile tl = decode(p, s, t);
       ring_dst[rs] = tl.dst;
       ring_bytes[rs] = tl.bytes;
       mbar_arrive_expect_tx(&bars[rs], tl.bytes);
@@ -331,6 +360,44 @@ __device__ void copy_bulk(const Params& p, const Plan& s, long long t0, long lon
     }
   }
   bulk_wait_all();
+}
+
+// Work items for the counter: out of place kItemTiles tiles each; in place whole runs, an item
+// ending at the run boundary nearest to a multiple of the mean tiles per run (at least
+// kItemTiles), so that most items are one run and few are empty.
+constexpr long long kItemTiles = 4;
+
+__device__ void copy_bulk_scheduled(const Params& p, const Plan& s, long long total, char* ring,
+                                    uint64_t* bars, char** ring_dst, uint32_t* ring_bytes) {
+  long long K = kItemTiles;
+  if (p.kv_in_place && s.runs_per_group > 0) {
+    const long long mean = (s.per_group + s.runs_per_group - 1) / s.runs_per_group;
+    K = mean > K ? mean : K;
+  }
+  const long long items = (total + K - 1) / K;
+  auto bound = [&](long long t) -> long long {
+    t = t < total ? t : total;
+    return p.kv_in_place ? run_boundary(p, s, t, total) : t;
+  };
+  long long cur = 0, end = 0;
+  unsigned ahead = atomicAdd(&p.sched[0], 1u);  // the next item, taken one item ahead
+  copy_bulk(p, s, [&](long long& t) -> bool {
+    while (cur >= end) {
+      if (static_cast<long long>(ahead) >= items) return false;
+      cur = bound(static_cast<long long>(ahead) * K);
+      end = bound(static_cast<long long>(ahead + 1) * K);
+      ahead = atomicAdd(&p.sched[0], 1u);
+    }
+    t = cur++;
+    return true;
+  }, ring, bars, ring_dst, ring_bytes);
+  // Every CTA has taken its last item once all have passed here: the last one clears the words.
+  __threadfence();
+  if (atomicAdd(&p.sched[1], 1u) == gridDim.x - 1) {
+    p.sched[0] = 0u;
+    p.sched[1] = 0u;
+    __threadfence();
+  }
 }
 
 // A coherent 16-byte global load.  In place the kernel writes bytes that other threads of the
@@ -497,7 +564,16 @@ __global__ void __launch_bounds__(kThreads) realign_kernel(const Params p) {
     if (threadIdx.x == 0) {
       for (int k = 0; k < p.stages; ++k) mbar_init(&bars[k], 1);
       fence_mbar_init();
-      if (t1 > t0) copy_bulk(p, s, t0, t1, ring, bars, ring_dst, ring_bytes);
+      if (p.sched) {
+        copy_bulk_scheduled(p, s, total, ring, bars, ring_dst, ring_bytes);
+      } else {
+        long long next = t0;
+        copy_bulk(p, s, [&](long long& t) -> bool {
+          if (next >= t1) return false;
+          t = next++;
+          return true;
+        }, ring, bars, ring_dst, ring_bytes);
+      }
     } else if (threadIdx.x >= 32) {
       const int per_cta = kThreads - 32;
       const int lt = threadIdx.x - 32;
@@ -665,6 +741,7 @@ int realign_common(const specdec_realign_args* a, bool in_place, void* stream) {
   if (a->D > SPECDEC_MAX_DRAFT || a->B > kMaxRows) return SPECDEC_ERR_UNSUPPORTED;
   if (a->copy_engine != 0 && a->copy_engine != 1) return SPECDEC_ERR_INVALID_ARG;
   if (a->flags & ~SPECDEC_REALIGN_PDL) return SPECDEC_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(a->schedule) % alignof(uint32_t)) return SPECDEC_ERR_INVALID_ARG;
   if (a->B == 0) return SPECDEC_OK;
   int st = check_view(a->src, 0);
   if (st) return st;
@@ -719,6 +796,7 @@ int realign_common(const specdec_realign_args* a, bool in_place, void* stream) {
   p.status = a->dev_status;
   p.kv_in_place = in_place ? 1 : 0;
   p.pdl = (a->flags & SPECDEC_REALIGN_PDL) ? 1 : 0;
+  p.sched = a->copy_engine == 0 ? reinterpret_cast<unsigned*>(a->schedule) : nullptr;
   return launch(p, static_cast<cudaStream_t>(stream));
 }
 

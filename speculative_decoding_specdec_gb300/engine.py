@@ -45,10 +45,12 @@ class Workspaces:
 
 class EqspecBatch:
     """``in_place=True`` keeps one K/V cache and realigns it in place (half the cache memory);
-    ids, mask and positions stay double-buffered."""
+    ids, mask and positions stay double-buffered.  ``scheduled=True`` (default) gives the
+    realignment its two scheduling words, so its CTAs take work items from a counter; False
+    gives every CTA a fixed share."""
 
     def __init__(self, layers, heads, head_dim, kv_dtype, B, D, cap, max_rounds, device="cuda",
-                 pad_id=0, in_place=False, pdl=False):
+                 pad_id=0, in_place=False, pdl=False, scheduled=True):
         self.L, self.H, self.hd, self.B, self.D, self.cap = layers, heads, head_dim, B, D, cap
         self.max_rounds = max_rounds
         self.pad_id = pad_id
@@ -69,6 +71,7 @@ class EqspecBatch:
         self.accept_len = self.hist[0, B + 1:2 * B + 1]
         self.out_token = self.hist[0, 2 * B + 1:]
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.schedule = torch.zeros(2, dtype=torch.int32, device=dev) if scheduled else None
         self.workspaces = Workspaces(dev)
         self.round = 0
         self.cur = 0
@@ -168,7 +171,8 @@ class EqspecBatch:
         specdec.realign(ks, kd, self.n_hist[r], self.w_hist[r], self.accept_len,
                         self.out_token, draft, self.ids[s], self.ids[d], self.mask[d],
                         self.pos[d], self.n_hist[r + 1], self.w_hist[r + 1], self.status,
-                        pad_id=self.pad_id, copy_engine=copy_engine, pdl=self.pdl, stream=stream)
+                        pad_id=self.pad_id, copy_engine=copy_engine, pdl=self.pdl, stream=stream,
+                        schedule=self.schedule)
         self.cur = d
         self.round = r + 1
 

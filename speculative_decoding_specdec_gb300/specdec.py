@@ -44,7 +44,7 @@ class RealignArgs(ctypes.Structure):
                 ("ids_dst", ctypes.c_void_p), ("mask_dst", ctypes.c_void_p),
                 ("pos_dst", ctypes.c_void_p), ("n_committed_dst", ctypes.c_void_p),
                 ("width_dst", ctypes.c_void_p), ("dev_status", ctypes.c_void_p),
-                ("flags", ctypes.c_int)]
+                ("flags", ctypes.c_int), ("schedule", ctypes.c_void_p)]
 
 
 class PoolArgs(ctypes.Structure):
@@ -334,11 +334,13 @@ def verify_sample_philox(target_logits, draft_logits, draft, seed, offset, tempe
 
 def realign(src, dst, n_committed, width, accept_len, out_token, draft, ids_src, ids_dst,
             mask_dst, pos_dst, n_committed_dst, width_dst, status, pad_id=0, copy_engine=0,
-            pdl=False, stream=None):
+            pdl=False, stream=None, schedule=None):
     """EQSPEC realignment from cache ``src`` into cache ``dst`` (both [L, 2, B, H, cap, hd]).
     Passing the same tensor as ``src`` and ``dst`` moves the K/V in place
     (specdec_realign_inplace); the metadata outputs stay separate.  ``pdl`` launches it as a
-    programmatic dependent of the kernel ahead of it (SPECDEC_REALIGN_PDL)."""
+    programmatic dependent of the kernel ahead of it (SPECDEC_REALIGN_PDL).  ``schedule``: None
+    (fixed equal shares per CTA) or a zero-filled int32 CUDA tensor of 2 elements that the call
+    leaves zero (work items taken from a counter; calls on other streams need their own)."""
     B, D = draft.shape
     in_place = src.data_ptr() == dst.data_ptr()
     a = RealignArgs()
@@ -346,6 +348,11 @@ def realign(src, dst, n_committed, width, accept_len, out_token, draft, ids_src,
     a.dst = kv_view(dst)
     a.B, a.D, a.pad_id, a.copy_engine = B, D, int(pad_id), int(copy_engine)
     a.flags = REALIGN_PDL if pdl else 0
+    if schedule is not None:
+        _need(schedule, torch.int32, "schedule")
+        if schedule.numel() < 2 or not schedule.is_contiguous():
+            raise ValueError("schedule needs 2 contiguous int32 elements")
+        a.schedule = schedule.data_ptr()
     for name, t in (("n_committed", n_committed), ("width", width), ("accept_len", accept_len),
                     ("out_token", out_token), ("draft", draft), ("ids_src", ids_src),
                     ("ids_dst", ids_dst), ("pos_dst", pos_dst),

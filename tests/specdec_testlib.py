@@ -13,19 +13,21 @@ def host_bits(t):
 
 def eqspec_rounds(L, H, hd, kv_dtype, B, D, V, rounds, prompt_lo, prompt_hi, seed,
                   copy_engine=0, alpha=0.6, logit_dtype=torch.float32, cap_extra=0,
-                  check_full_dst=True, in_place=False, pdl=False):
+                  check_full_dst=True, in_place=False, pdl=False, scheduled=True):
     """Greedy verify + realign for ``rounds`` rounds with tagged K/V; every round is compared
     with the oracle: accept lengths, tokens, lengths, width, ids, mask, position IDs, and the
     whole destination cache (the oracle leaves pad columns as they were, and so must the
     kernel).  With ``in_place`` the cache is one buffer realigned in place: the expected result
-    is the oracle's realignment into a copy of the source.  Returns the per-round accept
-    lengths."""
+    is the oracle's realignment into a copy of the source.  ``scheduled``: the realignment takes
+    work items from its scheduling words (checked back at zero after every call), else every
+    CTA a fixed share.  Returns the per-round accept lengths."""
     from speculative_decoding_specdec_gb300.engine import EqspecBatch
     gen = synth.make_gen(seed)
     n0 = synth.lengths_uniform(gen, B, prompt_lo, prompt_hi)
     prompts = [torch.randint(0, V, (int(n),), generator=gen).tolist() for n in n0]
     cap = int(n0.max()) + rounds * (D + 1) + D + 1 + cap_extra
-    eng = EqspecBatch(L, H, hd, kv_dtype, B, D, cap, rounds, in_place=in_place, pdl=pdl)
+    eng = EqspecBatch(L, H, hd, kv_dtype, B, D, cap, rounds, in_place=in_place, pdl=pdl,
+                      scheduled=scheduled)
     W = eng.start(prompts)
     eng.kv[0].fill_(-3.0)
     if not in_place:
@@ -50,6 +52,8 @@ def eqspec_rounds(L, H, hd, kv_dtype, B, D, V, rounds, prompt_lo, prompt_hi, see
         eng.realign(dd, copy_engine=copy_engine)
         torch.cuda.synchronize()
         assert int(eng.status.item()) == 0
+        if scheduled:
+            assert eng.schedule.tolist() == [0, 0]
         a, y = O.verify_greedy(logits.double().numpy(), draft.numpy())
         kv, ids, mask, pos, n, W = O.realign(src, dst_before, n, W, a, y, draft.numpy(), ids, 0)
         np.testing.assert_array_equal(eng.accept_len.cpu().numpy(), a)

@@ -121,6 +121,12 @@ def test_host_validation_codes():
     a.flags = 2                                                              # unknown flag
     assert L.specdec_realign(ctypes.byref(a), None) == sd.ERR_INVALID_ARG
     a.flags = 0
+    a.schedule = 4098                                        # scheduling words not 4-byte aligned
+    assert L.specdec_realign(ctypes.byref(a), None) == sd.ERR_INVALID_ARG
+    assert L.specdec_realign_inplace(ctypes.byref(a), None) == sd.ERR_INVALID_ARG
+    a.B = 0
+    assert L.specdec_realign(ctypes.byref(a), None) == sd.ERR_INVALID_ARG
+    a.schedule, a.B = None, 2
     # grouping
     assert L.specdec_group_by_length(None, -1, 8, 10, None, None, None, None, None, None, None) == sd.ERR_INVALID_ARG
     assert L.specdec_group_by_length(None, 5000, 8, 10, None, None, None, None, None, None, None) == sd.ERR_UNSUPPORTED

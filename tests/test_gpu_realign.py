@@ -58,6 +58,18 @@ def test_in_place(B, D, lo, hi, hd, dtype, L, H):
                   seed=50 + B + D, alpha=0.6, in_place=True)
 
 
+@pytest.mark.parametrize("in_place", [False, True])
+@pytest.mark.parametrize("B,lo,hi,L,H", [
+    (8, 20, 700, 2, 4),      # multi-tile runs with ragged last tiles
+    (300, 1, 6, 2, 2),       # many one-tile runs, zero-shift rows
+    (4, 300, 1300, 1, 2),    # runs of 2-6 tiles of 64 KB
+])
+def test_fixed_shares(in_place, B, lo, hi, L, H):
+    """Without scheduling words every CTA moves one fixed share of the tiles: same results."""
+    eqspec_rounds(L, H, 128, torch.bfloat16, B=B, D=5, V=300, rounds=3, prompt_lo=lo,
+                  prompt_hi=hi, seed=90 + B, alpha=0.7, in_place=in_place, scheduled=False)
+
+
 @pytest.mark.parametrize("copy_engine", [0, 1])
 def test_in_place_long_shifts(copy_engine):
     # prompts of very different lengths: runs of up to ~730 columns shifting both ways
@@ -225,3 +237,56 @@ def test_rounds_with_programmatic_dependent_launch(in_place):
     gives the oracle's result in every round."""
     eqspec_rounds(2, 4, 128, torch.bfloat16, B=8, D=5, V=500, rounds=5, prompt_lo=20,
                   prompt_hi=300, seed=11, alpha=0.7, in_place=in_place, pdl=True)
+
+
+@pytest.mark.parametrize("in_place", [False, True])
+def test_graph_replay_rounds(in_place):
+    """Rounds captured once into a CUDA graph (verification, then realignment as its programmatic
+    dependent, taking work items from the batch's scheduling words) and replayed: every round's
+    results, and both caches and the metadata after the last round, equal the oracle's.  The
+    words are back at zero after every launch, or a later round would skip its items."""
+    from speculative_decoding_specdec_gb300.engine import EqspecBatch
+    from specdec_testlib import host_bits
+    L, H, hd, B, D, V, R = 2, 4, 128, 8, 5, 500, 5
+    gen = synth.make_gen(21)
+    n0 = synth.lengths_uniform(gen, B, 20, 300)
+    prompts = [torch.randint(0, V, (int(n),), generator=gen).tolist() for n in n0]
+    cap = int(n0.max()) + R * (D + 1) + D + 1
+    eng = EqspecBatch(L, H, hd, torch.bfloat16, B, D, cap, R, in_place=in_place, pdl=True)
+    W = eng.start(prompts)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    for k in eng.kv:
+        k.view(torch.int16).random_(-32768, 32767, generator=g)
+    rounds = [synth.greedy_round(gen, B, D, V, 0.7, dtype=torch.bfloat16) for _ in range(R)]
+    dev_rounds = [(lg.cuda(), d.cuda()) for lg, d in rounds]
+    eng.workspaces.greedy(dev_rounds[0][0], dev_rounds[0][1])      # allocated before capture
+    bufs = [host_bits(k) for k in eng.kv]
+    ids = eng.ids[0].cpu().numpy()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for lg, d in dev_rounds:
+            eng.verify_greedy(lg, d)
+            eng.realign(d)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert int(eng.status.item()) == 0
+    assert eng.schedule.tolist() == [0, 0]
+    n = n0.numpy().astype(np.int64)
+    hist = eng.hist.cpu().numpy()
+    for r, (lg, d) in enumerate(rounds):
+        a, y = O.verify_greedy(lg.double().numpy(), d.numpy())
+        s_, d_ = (0, 0) if in_place else (r % 2, 1 - r % 2)
+        src = bufs[s_]
+        dst_before = src.copy() if in_place else bufs[d_]
+        kv, ids, mask, pos, n, W = O.realign(src, dst_before, n, W, a, y, d.numpy(), ids, 0)
+        bufs[d_] = kv
+        np.testing.assert_array_equal(hist[r, B + 1:2 * B + 1], a)
+        np.testing.assert_array_equal(hist[r, 2 * B + 1:], y)
+        np.testing.assert_array_equal(hist[r + 1, :B], n)
+        assert int(hist[r + 1, B]) == W
+    for k, exp in zip(eng.kv, bufs):
+        np.testing.assert_array_equal(host_bits(k), exp)
+    np.testing.assert_array_equal(eng.ids[eng.cur].cpu().numpy(), ids)
+    np.testing.assert_array_equal(eng.mask[eng.cur].cpu().numpy(), mask)
+    np.testing.assert_array_equal(eng.pos[eng.cur].cpu().numpy(), pos)
