@@ -23,8 +23,8 @@
 // Bytes moved = read + write of every surviving column, nothing else.
 //
 // Scheduling.  With a caller-owned schedule (two 32-bit words), the tiles are cut into work
-// items -- a few tiles, or whole runs in place -- and every CTA's elected thread takes the next
-// item from a counter as its ring frees up, keeping one item taken ahead.  Measured on GB300, the
+// items -- a few tiles, or one whole run in place, longest runs first -- and every CTA's elected
+// thread takes the next item from a counter as its ring frees up, keeping one item taken ahead.  Measured on GB300, the
 // SMs of one launch stream at unequal rates (the first CTA of an equal split finishes ~20 %
 // before the last), so a fixed split leaves SMs idle at the end while items from a counter keep
 // them all busy to the last item.  The last CTA to finish sets the words back to zero.  Without
@@ -60,6 +60,7 @@ constexpr int kMaxRows = 1024;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kWaitTries = 1u << 22;
 constexpr int kVecUnroll = 8;
+constexpr int kLptRows = 256;  // scheduled in place: longest-first item order up to this many rows
 
 enum Mode { kEqspec = 0, kPoolGather = 1, kPoolAppend = 2 };
 
@@ -107,8 +108,9 @@ struct Params {
   unsigned* sched;  // [2] next work item, finished CTAs (zero between calls); null: fixed shares
 };
 
-struct Plan {  // per-row plan, arrays in dynamic shared memory (7 ints per row)
+struct Plan {  // per-row plan, arrays in dynamic shared memory (8 ints per row)
   int *src_col, *dst_col, *ncols, *tiles, *prefix;
+  int* order;  // scheduled, in place: the rows that move, longest first (runs_per_group / H)
   int* aux;  // EQSPEC: N_b; pool: N_s
   int* acc;  // EQSPEC / append: a
   int W, Wp, per_group;
@@ -116,7 +118,7 @@ struct Plan {  // per-row plan, arrays in dynamic shared memory (7 ints per row)
 };
 
 __host__ __device__ constexpr size_t plan_bytes(int rows) {
-  return static_cast<size_t>(rows) * 7 * sizeof(int);
+  return static_cast<size_t>(rows) * 8 * sizeof(int);
 }
 
 __device__ __forceinline__ int src_row_of(int mode, int r) { return mode == kPoolGather ? 0 : r; }
@@ -253,6 +255,33 @@ __device__ bool build_plan(const Params& p, Plan& s, int* red) {
       s.per_group = incl;
       s.runs_per_group = runs;
     }
+    if (p.sched && p.kv_in_place && R > kLptRows) {  // the moving rows in index order
+      int nz = 0;
+      for (int r = r0; r < r1; ++r) nz += s.tiles[r] > 0;
+      int nz_incl = nz;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, nz_incl, o);
+        if (lane >= o) nz_incl += v;
+      }
+      int k = nz_incl - nz;
+      for (int r = r0; r < r1; ++r)
+        if (s.tiles[r] > 0) s.order[k++] = r;
+    }
+  }
+  if (p.sched && p.kv_in_place && R <= kLptRows) {
+    // The moving rows, longest runs first (ties: lower row first), so that the last work items
+    // a scheduled launch hands out are its shortest runs.
+    for (int r = threadIdx.x; r < R; r += kThreads) {
+      const int tr = s.tiles[r];
+      if (tr == 0) continue;
+      int rank = 0;
+      for (int q = 0; q < R; ++q) {
+        const int tq = s.tiles[q];
+        rank += (tq > tr) || (tq == tr && q < r);
+      }
+      s.order[rank] = r;
+    }
   }
   __syncthreads();
   return true;
@@ -362,31 +391,35 @@ __device__ void copy_bulk(const Params& p, const Plan& s, NextTile&& next_tile, 
   bulk_wait_all();
 }
 
-// Work items for the counter: out of place kItemTiles tiles each; in place whole runs, an item
-// ending at the run boundary nearest to a multiple of the mean tiles per run (at least
-// kItemTiles), so that most items are one run and few are empty.
+// Work items for the counter.  Out of place: kItemTiles consecutive tiles (runs may be cut).
+// In place: one run each (a run is moved by one CTA), the longest rows' runs first, so that the
+// items handed out last -- the ones that decide when the launch ends -- are the shortest.  The
+// first item of every CTA is its own index; later ones come from the counter, offset by the grid
+// size, so the launch does not start with every CTA on one atomic.
 constexpr long long kItemTiles = 4;
 
 __device__ void copy_bulk_scheduled(const Params& p, const Plan& s, long long total, char* ring,
                                     uint64_t* bars, char** ring_dst, uint32_t* ring_bytes) {
-  long long K = kItemTiles;
-  if (p.kv_in_place && s.runs_per_group > 0) {
-    const long long mean = (s.per_group + s.runs_per_group - 1) / s.runs_per_group;
-    K = mean > K ? mean : K;
-  }
-  const long long items = (total + K - 1) / K;
-  auto bound = [&](long long t) -> long long {
-    t = t < total ? t : total;
-    return p.kv_in_place ? run_boundary(p, s, t, total) : t;
-  };
+  const long long row_runs = 2LL * p.L * p.H;  // runs of one row (every (layer, k/v, head))
+  const long long items =
+      p.kv_in_place ? static_cast<long long>(s.runs_per_group / p.H) * row_runs
+                    : (total + kItemTiles - 1) / kItemTiles;
   long long cur = 0, end = 0;
-  unsigned ahead = atomicAdd(&p.sched[0], 1u);  // the next item, taken one item ahead
+  long long ahead = blockIdx.x;  // the next item
   copy_bulk(p, s, [&](long long& t) -> bool {
     while (cur >= end) {
-      if (static_cast<long long>(ahead) >= items) return false;
-      cur = bound(static_cast<long long>(ahead) * K);
-      end = bound(static_cast<long long>(ahead + 1) * K);
-      ahead = atomicAdd(&p.sched[0], 1u);
+      if (ahead >= items) return false;
+      if (p.kv_in_place) {
+        const long long q = ahead / row_runs, rem = ahead - q * row_runs;
+        const long long g = rem / p.H, h = rem - g * p.H;
+        const int r = s.order[q];
+        cur = g * s.per_group + s.prefix[r] + h * s.tiles[r];
+        end = cur + s.tiles[r];
+      } else {
+        cur = ahead * kItemTiles;
+        end = cur + kItemTiles < total ? cur + kItemTiles : total;
+      }
+      ahead = static_cast<long long>(atomicAdd(&p.sched[0], 1u)) + gridDim.x;
     }
     t = cur++;
     return true;
@@ -547,6 +580,7 @@ __global__ void __launch_bounds__(kThreads) realign_kernel(const Params p) {
     s.prefix = a + 4 * p.R;
     s.aux = a + 5 * p.R;
     s.acc = a + 6 * p.R;
+    s.order = a + 7 * p.R;
   }
   __syncthreads();
   if (!build_plan(p, s, red)) return;
