@@ -545,7 +545,8 @@ def run_pool(args, rank, ws):
     if need > 0.85 * free:
         raise SystemExit(f"pool arena needs {need / 1e9:.0f} GB, {free / 1e9:.0f} GB free: "
                          f"fewer rounds (--steps/--warmup)")
-    pool = ExspecPool(w.layers, w.heads, w.head_dim, w.kv_dtype, prompts, w.D, R, device=dev)
+    pool = ExspecPool(w.layers, w.heads, w.head_dim, w.kv_dtype, prompts, w.D, R, device=dev,
+                      scheduled=args.realign_schedule == "counter")
     g = torch.Generator(device=dev).manual_seed(w.seed)
     logits, drafts = [], []
     for _ in range(R):
@@ -650,7 +651,8 @@ def run_serving(args, rank, ws):
     if need > 0.85 * free:
         raise SystemExit(f"serving pool needs {need / 1e9:.0f} GB, {free / 1e9:.0f} GB free")
     pool = SequencePool(w.layers, w.heads, w.head_dim, w.kv_dtype, S, arena_cols, D, max_len,
-                        batch_size=8, window=args.window, eos_id=2, device=dev)
+                        batch_size=8, window=args.window, eos_id=2, device=dev,
+                        scheduled=args.realign_schedule == "counter")
     alpha = (torch.rand(S, generator=gen) * 0.4 + 0.5).to(dev)    # acceptance U[0.5, 0.9] per slot
     g = torch.Generator(device=dev).manual_seed(w.seed)
     logits, drafts = [], []

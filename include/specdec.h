@@ -401,6 +401,7 @@ typedef struct {
   uint8_t* slot_state;          /* [S] specdec_slot_state of each slot */
   const int32_t* slot_limit;    /* [S] length limit of each slot */
   int32_t eos_id;               /* end-of-sequence token id (< 0: length limit only) */
+  uint32_t* schedule;           /* NULL, or [2] scheduling words, as in specdec_realign_args */
 } specdec_pool_args;
 
 int specdec_pool_gather(const specdec_pool_args* args, void* stream);

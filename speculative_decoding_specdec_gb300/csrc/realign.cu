@@ -723,6 +723,7 @@ int pool_common(const specdec_pool_args* a, Params& p, bool append) {
     return SPECDEC_ERR_INVALID_ARG;
   if (append && (!a->accept_len || !a->out_token || !a->draft)) return SPECDEC_ERR_INVALID_ARG;
   if (append && a->slot_state && !a->slot_limit) return SPECDEC_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(a->schedule) % alignof(uint32_t)) return SPECDEC_ERR_INVALID_ARG;
   uintptr_t alo, ahi, slo, shi;
   view_span(ar, alo, ahi);
   view_span(sc, slo, shi);
@@ -760,6 +761,7 @@ int pool_common(const specdec_pool_args* a, Params& p, bool append) {
   p.slot_limit = a->slot_limit;
   p.eos_id = a->eos_id;
   p.status = a->dev_status;
+  p.sched = reinterpret_cast<unsigned*>(a->schedule);
   return SPECDEC_OK;
 }
 

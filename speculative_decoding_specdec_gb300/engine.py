@@ -71,7 +71,7 @@ class EqspecBatch:
         self.accept_len = self.hist[0, B + 1:2 * B + 1]
         self.out_token = self.hist[0, 2 * B + 1:]
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.schedule = torch.zeros(2, dtype=torch.int32, device=dev) if scheduled else None
+        self.sched_words = torch.zeros(2, dtype=torch.int32, device=dev) if scheduled else None
         self.workspaces = Workspaces(dev)
         self.round = 0
         self.cur = 0
@@ -172,7 +172,7 @@ class EqspecBatch:
                         self.out_token, draft, self.ids[s], self.ids[d], self.mask[d],
                         self.pos[d], self.n_hist[r + 1], self.w_hist[r + 1], self.status,
                         pad_id=self.pad_id, copy_engine=copy_engine, pdl=self.pdl, stream=stream,
-                        schedule=self.schedule)
+                        schedule=self.sched_words)
         self.cur = d
         self.round = r + 1
 
@@ -261,7 +261,7 @@ class ExspecPool:
     """
 
     def __init__(self, layers, heads, head_dim, kv_dtype, prompts, D, rounds, batch_size=8,
-                 device="cuda", pad_id=0):
+                 device="cuda", pad_id=0, scheduled=True):
         dev = torch.device(device)
         self.S = len(prompts)
         self.D, self.bs, self.pad_id = D, batch_size, pad_id
@@ -298,6 +298,7 @@ class ExspecPool:
         self.accept_len = torch.zeros(self.S, **i32)
         self.out_token = torch.zeros(self.S, **i32)
         self.status = torch.zeros(1, **i32)
+        self.sched_words = torch.zeros(2, **i32) if scheduled else None  # gather/append work items
         self.workspaces = Workspaces(dev)
         self._host = torch.zeros(2 + (self.S + 1) + self.S, dtype=torch.int32).pin_memory()
 
@@ -334,7 +335,8 @@ class ExspecPool:
         specdec.pool_gather(self.arena, self.scratch, rows, self.D, self.slot_col, self.slot_cap,
                             self.slot_len, self.pool_ids, self.batch_len[:n], self.width,
                             self.status, self.scratch_ids, self.scratch_mask, self.scratch_pos,
-                            pad_id=self.pad_id, in_place=uniform, stream=stream)
+                            pad_id=self.pad_id, in_place=uniform, stream=stream,
+                            schedule=self.sched_words)
 
     def append(self, off, n, uniform, draft, stream=None):
         """Commit batch perm[off:off+n] back to its slots (pool-wide accept lengths and tokens)."""
@@ -342,7 +344,8 @@ class ExspecPool:
         specdec.pool_append(self.arena, self.scratch, rows, self.D, self.slot_col, self.slot_cap,
                             self.slot_len, self.pool_ids, self.batch_len[:n], self.width,
                             self.accept_len, self.out_token, draft, self.status,
-                            in_place=uniform, by_slot=True, stream=stream)
+                            in_place=uniform, by_slot=True, stream=stream,
+                            schedule=self.sched_words)
 
 
 class SequencePool:
@@ -364,7 +367,7 @@ class SequencePool:
     """
 
     def __init__(self, layers, heads, head_dim, kv_dtype, S, arena_cols, D, max_len,
-                 batch_size=8, window=0, eos_id=-1, device="cuda", pad_id=0):
+                 batch_size=8, window=0, eos_id=-1, device="cuda", pad_id=0, scheduled=True):
         dev = torch.device(device)
         self.S, self.D, self.bs, self.window = S, D, batch_size, window
         self.eos_id, self.pad_id, self.max_len = eos_id, pad_id, max_len
@@ -398,6 +401,7 @@ class SequencePool:
         self.accept_len = torch.zeros(S, **i32)
         self.out_token = torch.zeros(S, **i32)
         self.status = torch.zeros(1, **i32)
+        self.sched_words = torch.zeros(2, **i32) if scheduled else None  # gather/append work items
         self.workspaces = Workspaces(dev)
         # schedule readback: counts | offsets | uniform | finished | reason | slot_len | perm
         self._host = torch.zeros(4 + (S + 1) + 5 * S, dtype=torch.int32).pin_memory()
@@ -502,7 +506,7 @@ class SequencePool:
                             self.slot_col, self.slot_cap, self.slot_len, self.pool_ids,
                             self.batch_len[:n], self.width, self.status, self.scratch_ids,
                             self.scratch_mask, self.scratch_pos, pad_id=self.pad_id,
-                            in_place=uniform, stream=stream)
+                            in_place=uniform, stream=stream, schedule=self.sched_words)
 
     def append(self, off, n, uniform, draft, stream=None):
         """Commit batch perm[off:off+n] back to its slots and retire finished sequences."""
@@ -511,4 +515,4 @@ class SequencePool:
                             self.batch_len[:n], self.width, self.accept_len, self.out_token,
                             draft, self.status, in_place=uniform, by_slot=True,
                             slot_state=self.slot_state, slot_limit=self.slot_limit,
-                            eos_id=self.eos_id, stream=stream)
+                            eos_id=self.eos_id, stream=stream, schedule=self.sched_words)

@@ -59,7 +59,7 @@ class PoolArgs(ctypes.Structure):
                 ("out_token", ctypes.c_void_p), ("draft", ctypes.c_void_p),
                 ("by_slot", ctypes.c_int), ("dev_status", ctypes.c_void_p),
                 ("slot_state", ctypes.c_void_p), ("slot_limit", ctypes.c_void_p),
-                ("eos_id", ctypes.c_int32)]
+                ("eos_id", ctypes.c_int32), ("schedule", ctypes.c_void_p)]
 
 
 class ScheduleArgs(ctypes.Structure):
@@ -332,6 +332,16 @@ def verify_sample_philox(target_logits, draft_logits, draft, seed, offset, tempe
         _stream(stream)), "specdec_verify_sample_philox")
 
 
+def _schedule(t):
+    """Device address of a pair of scheduling words (None: fixed shares)."""
+    if t is None:
+        return None
+    _need(t, torch.int32, "schedule")
+    if t.numel() < 2 or not t.is_contiguous():
+        raise ValueError("schedule needs 2 contiguous int32 elements")
+    return t.data_ptr()
+
+
 def realign(src, dst, n_committed, width, accept_len, out_token, draft, ids_src, ids_dst,
             mask_dst, pos_dst, n_committed_dst, width_dst, status, pad_id=0, copy_engine=0,
             pdl=False, stream=None, schedule=None):
@@ -348,11 +358,7 @@ def realign(src, dst, n_committed, width, accept_len, out_token, draft, ids_src,
     a.dst = kv_view(dst)
     a.B, a.D, a.pad_id, a.copy_engine = B, D, int(pad_id), int(copy_engine)
     a.flags = REALIGN_PDL if pdl else 0
-    if schedule is not None:
-        _need(schedule, torch.int32, "schedule")
-        if schedule.numel() < 2 or not schedule.is_contiguous():
-            raise ValueError("schedule needs 2 contiguous int32 elements")
-        a.schedule = schedule.data_ptr()
+    a.schedule = _schedule(schedule)
     for name, t in (("n_committed", n_committed), ("width", width), ("accept_len", accept_len),
                     ("out_token", out_token), ("draft", draft), ("ids_src", ids_src),
                     ("ids_dst", ids_dst), ("pos_dst", pos_dst),
@@ -409,10 +415,12 @@ def _pool_args(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, 
 
 def pool_gather(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len, width,
                 status, scratch_ids=None, scratch_mask=None, scratch_pos=None, pad_id=0,
-                in_place=False, stream=None):
-    """Gather pool slots ``rows`` into the padded batch buffer ``scratch`` (see specdec.h)."""
+                in_place=False, stream=None, schedule=None):
+    """Gather pool slots ``rows`` into the padded batch buffer ``scratch`` (see specdec.h).
+    ``schedule``: as in ``realign``."""
     a = _pool_args(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len,
                    width, status, pad_id, in_place)
+    a.schedule = _schedule(schedule)
     if not in_place:
         for t, n, dt in ((scratch_ids, "scratch_ids", torch.int32),
                          (scratch_mask, "scratch_mask", torch.uint8),
@@ -428,13 +436,14 @@ def pool_gather(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids,
 
 def pool_append(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len, width,
                 accept_len, out_token, draft, status, in_place=False, by_slot=False,
-                slot_state=None, slot_limit=None, eos_id=-1, stream=None):
+                slot_state=None, slot_limit=None, eos_id=-1, stream=None, schedule=None):
     """Append a verified batch back to its pool slots (see specdec.h).  With ``by_slot`` the
     accept lengths, tokens and drafts are pool-wide arrays indexed by slot.  With ``slot_state``
     (and ``slot_limit``) finished sequences are retired: end-of-sequence token ``eos_id`` or the
-    length limit."""
+    length limit.  ``schedule``: as in ``realign``."""
     a = _pool_args(arena, scratch, rows, D, slot_col, slot_cap, slot_len, pool_ids, batch_len,
                    width, status, 0, in_place)
+    a.schedule = _schedule(schedule)
     a.by_slot = int(bool(by_slot))
     for name, t in (("accept_len", accept_len), ("out_token", out_token), ("draft", draft)):
         _need(t, torch.int32, name)

@@ -53,7 +53,7 @@ def eqspec_rounds(L, H, hd, kv_dtype, B, D, V, rounds, prompt_lo, prompt_hi, see
         torch.cuda.synchronize()
         assert int(eng.status.item()) == 0
         if scheduled:
-            assert eng.schedule.tolist() == [0, 0]
+            assert eng.sched_words.tolist() == [0, 0]
         a, y = O.verify_greedy(logits.double().numpy(), draft.numpy())
         kv, ids, mask, pos, n, W = O.realign(src, dst_before, n, W, a, y, draft.numpy(), ids, 0)
         np.testing.assert_array_equal(eng.accept_len.cpu().numpy(), a)

@@ -25,7 +25,10 @@ def _pool(S, cap, L, H, hd, V, gen, lo, hi):
                 slot_len=i32(n.numpy()), pool_ids=pool_ids.to(dev), toks=toks)
 
 
-def test_gather_append_rounds_match_oracle():
+@pytest.mark.parametrize("scheduled", [False, True])
+def test_gather_append_rounds_match_oracle(scheduled):
+    """Gather / append against the oracle, with fixed CTA shares or with work items taken from
+    a pair of scheduling words (back at zero after every call)."""
     import speculative_decoding_specdec_gb300.specdec as sd
     gen = synth.make_gen(21)
     S, cap, L, H, hd, D, V, R = 12, 80, 2, 3, 64, 4, 50, 5
@@ -39,6 +42,7 @@ def test_gather_append_rounds_match_oracle():
     blen = torch.zeros(R, dtype=torch.int32, device=dev)
     width = torch.zeros(1, dtype=torch.int32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
+    sched = torch.zeros(2, dtype=torch.int32, device=dev) if scheduled else None
     rng = np.random.default_rng(2)
     for _ in range(6):
         k = int(rng.integers(1, R + 1))
@@ -49,9 +53,10 @@ def test_gather_append_rounds_match_oracle():
         ids_np = P["pool_ids"].cpu().numpy()
         sc0 = scratch.cpu().numpy()
         sd.pool_gather(P["arena"], scratch, rows, D, P["slot_col"], P["slot_cap"], P["slot_len"],
-                       P["pool_ids"], blen, width, st, s_ids, s_mask, s_pos)
+                       P["pool_ids"], blen, width, st, s_ids, s_mask, s_pos, schedule=sched)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
+        assert sched is None or sched.tolist() == [0, 0]
         exp_sc, W, eids, emask, epos = O.pool_gather(ar0, np.arange(S) * cap, n_np, rows_np.tolist(),
                                                    sc0, 0, ids_np)
         assert int(width.item()) == W
@@ -72,9 +77,10 @@ def test_gather_append_rounds_match_oracle():
         ga = torch.as_tensor(a, device=dev)
         gy = torch.as_tensor(y, device=dev)
         sd.pool_append(P["arena"], scratch, rows, D, P["slot_col"], P["slot_cap"], P["slot_len"],
-                       P["pool_ids"], blen, width, ga, gy, draft.to(dev), st)
+                       P["pool_ids"], blen, width, ga, gy, draft.to(dev), st, schedule=sched)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
+        assert sched is None or sched.tolist() == [0, 0]
         exp_ar, exp_len, exp_ids = O.pool_append(ar1, np.arange(S) * cap, n_np, rows_np.tolist(),
                                                  sc1, W, a, y, draft.numpy(), ids_np)
         np.testing.assert_array_equal(P["arena"][:, :, 0].cpu().numpy(), exp_ar)

@@ -271,7 +271,7 @@ def test_graph_replay_rounds(in_place):
     graph.replay()
     torch.cuda.synchronize()
     assert int(eng.status.item()) == 0
-    assert eng.schedule.tolist() == [0, 0]
+    assert eng.sched_words.tolist() == [0, 0]
     n = n0.numpy().astype(np.int64)
     hist = eng.hist.cpu().numpy()
     for r, (lg, d) in enumerate(rounds):
