@@ -93,12 +93,31 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
 }
 
 // Equal contiguous shares of `units` units over G CTAs (G <= units, so no share is empty).
+// narrow: units * G < 2^32, so every product and quotient below fits 32-bit unsigned arithmetic
+// (a 64-bit division is a long dependent instruction sequence on the GPU; these sit on the
+// critical path of a launch's start and of its per-row merge).
 struct Split {
   long long units;
   int G;
-  __device__ __host__ long long start(int c) const { return units * c / G; }
+  int narrow;
+  __device__ __host__ long long start(int c) const {
+    if (narrow)
+      return static_cast<long long>(static_cast<unsigned>(units) * static_cast<unsigned>(c) /
+                                    static_cast<unsigned>(G));
+    return units * c / G;
+  }
   // The CTA whose share holds unit u: the largest c with start(c) <= u.
-  __device__ int owner(long long u) const { return static_cast<int>(((u + 1) * G - 1) / units); }
+  __device__ int owner(long long u) const {
+    if (narrow)
+      return static_cast<int>((static_cast<unsigned>(u + 1) * static_cast<unsigned>(G) - 1u) /
+                              static_cast<unsigned>(units));
+    return static_cast<int>(((u + 1) * G - 1) / units);
+  }
+  // u / d for 0 <= u <= units and d >= 1.
+  __device__ long long div(long long u, int d) const {
+    if (narrow) return static_cast<long long>(static_cast<unsigned>(u) / static_cast<unsigned>(d));
+    return u / d;
+  }
 };
 
 struct GreedyArgs {
@@ -150,7 +169,7 @@ __device__ void merge_and_decide(const GreedyArgs& A, const unsigned long long* 
     fence_acq_rel_gpu();
   }
   __syncthreads();
-  const long long b0 = g0 / Q, b1 = g1 / Q;
+  const long long b0 = A.split.div(g0, Q), b1 = A.split.div(g1, Q);
   const int nb = static_cast<int>(b1 - b0 + 1);
   for (int k = tid; k < nb; k += NT) {
     const long long b = b0 + k;
@@ -196,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 2) greedy_kernel(const GreedyArgs A)
   const int c = blockIdx.x;
   const int tid = threadIdx.x;
   const long long u0 = A.split.start(c), u1 = A.split.start(c + 1);
-  const long long g0 = u0 / A.RU, g1 = (u1 - 1) / A.RU;  // first and last global row touched
+  const long long g0 = A.split.div(u0, A.RU), g1 = A.split.div(u1 - 1, A.RU);  // rows touched
   const int nseg = static_cast<int>(g1 - g0 + 1);
   if (nseg > kMaxSegs) {  // excluded by the launch geometry
     if (tid == 0) set_status(A.status, SPECDEC_ERR_UNSUPPORTED);
@@ -298,22 +317,29 @@ __global__ void __launch_bounds__(kRingThreads, 1) greedy_ring_kernel(const Gree
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int RU = A.RU;
   const long long u0 = A.split.start(c), u1 = A.split.start(c + 1);
-  const long long g0 = u0 / RU, g1 = (u1 - 1) / RU;  // first and last global row touched
+  const long long g0 = A.split.div(u0, RU), g1 = A.split.div(u1 - 1, RU);  // rows touched
   const int nseg = static_cast<int>(g1 - g0 + 1);
   if (nseg > kMaxSegs) {  // excluded by the launch geometry
     if (tid == 0) set_status(A.status, SPECDEC_ERR_UNSUPPORTED);
     return;
   }
-  for (int s = tid; s < nseg; s += kRingThreads) s_key[s] = 0ull;
-  if (tid == 0) {
-    s_fail = 0;
-    for (int k = 0; k < kRingStages; ++k) {
-      mbar_init(&full[k], 1);
-      mbar_init(&empty[k], kRingWarps);
+  // The producer warp sets up the ring's barriers and goes straight on to its copies; the
+  // consumers clear the row keys and wait (named barrier 1) until the barriers exist.
+  if (warp == kRingWarps) {
+    if (lane == 0) {
+      s_fail = 0;
+      for (int k = 0; k < kRingStages; ++k) {
+        mbar_init(&full[k], 1);
+        mbar_init(&empty[k], kRingWarps);
+      }
+      fence_mbar_init();
     }
-    fence_mbar_init();
+    __syncwarp();
+    named_bar_arrive(1, kRingThreads);
+  } else {
+    for (int s = tid; s < nseg; s += kRingConsumers) s_key[s] = 0ull;
+    named_bar_sync(1, kRingThreads);
   }
-  __syncthreads();
   const char* base = static_cast<const char*>(A.logits);  // unit u at base + 16 u
   // Segment k: units [lo, hi) of row g0 + k.
   auto seg_lo = [&](int k) { return static_cast<int>(max(u0, (g0 + k) * RU) - (g0 + k) * RU); };
@@ -449,7 +475,7 @@ int launch(const void* logits, int B, int D, int V, long long row_stride, const 
   A.step_rows = kThreads / g.RU;
   A.step_off = kThreads % g.RU;
   A.row_stride = row_stride;
-  A.split = Split{g.units, g.G};
+  A.split = Split{g.units, g.G, g.units * g.G < (1LL << 32) ? 1 : 0};
   A.draft = draft;
   A.accept_len = accept_len;
   A.out_token = out_token;

@@ -354,15 +354,20 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
     }
   };
 
-  for (int k = tid; k < kMaxQ * kWarps; k += kThreads) {
-    (&po[0][0])[k] = kOffsetNone;
-    (&ps[0][0])[k] = 0.f;
-  }
+  // The producer warp sets up the ring's barriers and the stream plan and goes straight on to
+  // its copies; the consumers clear the partials, read the keep bounds and wait (named barrier
+  // 1) until the barriers and the plan exist.
   const bool filter = A.keep != nullptr;
-  for (int k = tid; k < Q; k += kThreads)
-    s_keep[k] = keep_threshold(filter ? A.keep[static_cast<long long>(b) * Q + k]
-                                      : make_uint2(0u, 0x7fffffffu));
-  if (tid == 0) {
+  if (warp != kWarps) {
+    for (int k = tid; k < kMaxQ * kWarps; k += kConsumers) {
+      (&po[0][0])[k] = kOffsetNone;
+      (&ps[0][0])[k] = 0.f;
+    }
+    for (int k = tid; k < Q; k += kConsumers)
+      s_keep[k] = keep_threshold(filter ? A.keep[static_cast<long long>(b) * Q + k]
+                                        : make_uint2(0u, 0x7fffffffu));
+    named_bar_sync(1, kThreads);
+  } else if (lane == 0) {
     s_bad = 0;
     s_found = 0;
     s_last = -1;
@@ -379,19 +384,28 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
     if (contiguous) {
       const long long nt = static_cast<long long>(D + 1) * V;  // target scores of this row
       const long long units = (nt + static_cast<long long>(D) * V) / VN;
-      const long long e0 = units * rank / C * VN, e1 = units * (rank + 1) / C * VN;
+      // 32-bit quotients where they fit (a 64-bit division is a long dependent sequence, and
+      // these precede this CTA's first copy)
+      const bool narrow = units * C < (1LL << 32) && nt + static_cast<long long>(D) * V < (1LL << 32);
+      auto qd = [&](long long a, long long d) -> long long {
+        return narrow ? static_cast<long long>(static_cast<unsigned>(a) / static_cast<unsigned>(d))
+                      : a / d;
+      };
+      const long long e0 = qd(units * rank, C) * VN, e1 = qd(units * (rank + 1), C) * VN;
       if (e0 < nt) {  // the target part of the range
         const long long hi = min(e1, nt);
+        const long long r0 = qd(e0, V);
         plan.blk[plan.nblk++] = StreamBlock{reinterpret_cast<const char*>(row_ptr(0) + e0),
-                                            static_cast<int>(hi - e0), static_cast<int>(e0 / V),
-                                            static_cast<int>(e0 % V)};
+                                            static_cast<int>(hi - e0), static_cast<int>(r0),
+                                            static_cast<int>(e0 - r0 * V)};
       }
       if (e1 > nt) {  // the draft part
         const long long lo = max(e0, nt) - nt, hi = e1 - nt;
+        const long long r0 = qd(lo, V);
         plan.blk[plan.nblk++] = StreamBlock{reinterpret_cast<const char*>(row_ptr(D + 1) + lo),
                                             static_cast<int>(hi - lo),
-                                            D + 1 + static_cast<int>(lo / V),
-                                            static_cast<int>(lo % V)};
+                                            D + 1 + static_cast<int>(r0),
+                                            static_cast<int>(lo - r0 * V)};
       }
     } else if (kVec && body > 0) {
       for (int q = 0; q < Q; ++q)
@@ -400,7 +414,10 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
     }
     plan.finish(Cfg<W>::kChunkBytes / static_cast<int>(sizeof(T)), kRingBytes);
   }
-  __syncthreads();
+  if (warp == kWarps) {
+    __syncwarp();
+    named_bar_arrive(1, kThreads);
+  }
 
   // ---------------------------------------------------------------- phase 1: normalisers
   if (kVec) {
