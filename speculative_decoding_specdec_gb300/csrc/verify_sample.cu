@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
   __shared__ float slice_sum[2];  // this CTA's residual total (second slot: fallback to p)
   __shared__ double s_R, s_P;
   __shared__ float s_tl, s_inv, s_iz, s_iw;
-  __shared__ int s_owner, s_valid;
+  __shared__ int s_owner, s_valid, s_chunk;
   __shared__ int s_a, s_bad, s_found, s_y, s_last, s_fail;
   __shared__ __align__(8) uint64_t full[kMaxRingStages], empty[kMaxRingStages], pbar;
   __shared__ StreamPlan plan;
@@ -370,6 +370,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
   } else if (lane == 0) {
     s_bad = 0;
     s_found = 0;
+    s_chunk = -1;
     s_last = -1;
     s_fail = 0;
     for (int k = 0; k < kMaxRingStages; ++k) {
@@ -753,29 +754,52 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
   const bool valid = s_valid != 0;
   if (s_owner) {
     const float tl_ = s_tl;
-    const float E = tid ? incl[tid - 1] : 0.f;
-    if (E <= tl_ && tl_ < incl[tid]) {
-      float run = E;
-      int y = -1, last = -1;
-      for (int i = c0; i < c1 && y < 0; i += VN) {
-        float r[VN];
-        if (i + VN <= c1) {
-          r_vec(i, r);
-        } else {
-#pragma unroll
-          for (int k = 0; k < VN; ++k) r[k] = (i + k < c1) ? r_at(i + k) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < VN; ++k) {
-          if (y < 0 && i + k < c1) {
-            if (r[k] > 0.f) last = i + k;
-            run += r[k];
-            if (run > tl_) y = i + k;
-          }
-        }
+    {
+      const float E = tid ? incl[tid - 1] : 0.f;
+      if (E <= tl_ && tl_ < incl[tid]) s_chunk = tid;  // the thread chunk that holds t
+    }
+    __syncthreads();
+    const int oc = s_chunk;
+    if (oc >= 0 && warp == oc / 32) {
+      // The owning chunk [o0, o1) is searched by the whole warp: lane l sums its m entries, a
+      // warp scan places the lanes, and the lane whose entries hold t walks them in order.
+      const int o0 = min(len, oc * K), o1 = min(len, o0 + K);
+      const int m = (o1 - o0 + 31) / 32;
+      const int l0 = min(o1, o0 + lane * m), l1 = min(o1, l0 + m);
+      float part = 0.f;
+      int last = -1;
+      for (int i = l0; i < l1; ++i) {
+        const float r = r_at(i);
+        part += r;
+        if (r > 0.f) last = i;
       }
-      if (y < 0) y = last;  // rounding inside the chunk: its last nonzero entry
-      if (y >= 0) { s_y = s0 + y; s_found = 1; }
+      float inc = part;
+#pragma unroll
+      for (int k = 1; k < 32; k <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, inc, k);
+        if (lane >= k) inc += t;
+      }
+      const float E = oc ? incl[oc - 1] : 0.f;
+      const unsigned hit = __ballot_sync(0xffffffffu, E + inc > tl_);
+      int y = -1;
+      if (hit) {
+        const int hl = __ffs(static_cast<int>(hit)) - 1;
+        if (lane == hl) {
+          float run = E + (inc - part);
+          for (int i = l0; i < l1 && y < 0; ++i) {
+            run += r_at(i);
+            if (run > tl_) y = i;
+          }
+          if (y < 0) y = last;  // rounding inside the lane's entries: its last nonzero one
+        }
+        y = __shfl_sync(0xffffffffu, y, hl);
+      }
+      if (y < 0) {  // rounding past the chunk's end: the chunk's last nonzero entry
+#pragma unroll
+        for (int k = 16; k > 0; k >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, k));
+        y = last;
+      }
+      if (lane == 0 && y >= 0) { s_y = s0 + y; s_found = 1; }
     }
     __syncthreads();
     if (!s_found) {  // t rounded past this slice's scan: the slice's last nonzero entry
