@@ -15,24 +15,25 @@
 // run (l, kv, r, h) moves ncols_r columns of col_bytes from src column src_col_r to dst column
 // dst_col_r.  Every CTA recomputes the per-row plan from a few device ints (so no host
 // synchronisation is needed) and cuts every run into tiles of at most `tile` bytes.  The tiles
-// are numbered (l, kv, row, head, chunk) -- memory order -- and every CTA of a persistent grid
-// (a multiple of the SM count) takes one contiguous range of them.  One elected thread streams
-// its range through a ring of shared-memory stages with cp.async.bulk global->shared
+// are numbered (l, kv, row, head, chunk) -- memory order -- and the CTAs of a persistent grid
+// (a multiple of the SM count) share them out (see Scheduling).  One elected thread streams
+// its tiles through a ring of shared-memory stages with cp.async.bulk global->shared
 // (completion on an mbarrier) and cp.async.bulk shared->global (bulk groups), keeping
 // stages-1 loads in flight; the other warps meanwhile write the ids, mask and position IDs.
 // Bytes moved = read + write of every surviving column, nothing else.
 //
 // Scheduling.  With a caller-owned schedule (two 32-bit words), the tiles are cut into work
 // items -- a few tiles, or one whole run in place, longest runs first -- and every CTA's elected
-// thread takes the next item from a counter as its ring frees up, keeping one item taken ahead.  Measured on GB300, the
-// SMs of one launch stream at unequal rates (the first CTA of an equal split finishes ~20 %
-// before the last), so a fixed split leaves SMs idle at the end while items from a counter keep
-// them all busy to the last item.  The last CTA to finish sets the words back to zero.  Without
-// a schedule every CTA takes one fixed, contiguous share.
+// thread takes the next item from a counter as its ring frees up, keeping one item taken
+// ahead.  Measured on GB300, the SMs of one launch stream at unequal rates (the first CTA of an
+// equal split finishes ~20 % before the last), so a fixed split leaves SMs idle at the end while
+// items from a counter keep them all busy to the last item.  The last CTA to finish sets the
+// words back to zero.  Without a schedule every CTA takes one fixed, contiguous share of the
+// tiles (in place: ending at the nearest run boundary).
 //
 // In place (EQSPEC, one K/V buffer): a run moves within its own head row by the row's shift
-// s = dst_col - src_col.  Every run is handled by one CTA (grid shares end at the nearest run
-// boundary), which takes its tiles in ascending column order when s < 0 and descending when s > 0;
+// s = dst_col - src_col.  Every run is handled by one CTA, which takes its tiles in ascending
+// column order when s < 0 and descending when s > 0;
 // since a tile is stored only after its own load and every earlier load has landed, no store
 // reaches source bytes that are still to be read.  Rows with s = 0 move nothing.
 #include <climits>
