@@ -884,6 +884,76 @@ def time_oracle(wname, budget_s=15.0, max_rounds=60):
     return rounds / total, rounds, Ls, w
 
 
+def time_cpu_parallel(wname, budget_s=8.0, max_rounds=60, layers_sample=2):
+    """Rounds/s of the row-parallel C++ baseline (oracle/specdec_cpu_parallel.cpp, one
+    std::thread per host core) on the oracle's sample of the workload: verification of every
+    row (greedy or sampled), realignment of ``layers_sample`` layers scaled to all layers."""
+    import numpy as np
+    import torch
+    from oracle import _build_cpu
+    from speculative_decoding_specdec_gb300 import synth
+
+    w = synth.WORKLOADS[wname]
+    lib = _build_cpu.load()
+    threads = len(os.sched_getaffinity(0)) or 1  # the cores this process may run on
+    gen = synth.make_gen(w.seed * 1000)
+    n = w.prompt_lengths(gen).numpy().astype(np.int32)
+    W = int(n.max())
+    cap = w.capacity(W, rounds=max_rounds)
+    Ls = min(layers_sample, w.layers)
+    rng = np.random.default_rng(0)
+    es = 2 if w.kv_dtype == torch.bfloat16 else 4
+    kv = [rng.integers(-30000, 30000, size=(Ls, 2, w.B, w.heads, cap, w.head_dim * es // 2),
+                       dtype=np.int16) for _ in range(2)]
+    ids = [np.zeros((w.B, cap), np.int32) for _ in range(2)]
+    mask = np.zeros((w.B, cap), np.uint8)
+    pos = np.zeros((w.B, cap), np.int32)
+    n_out = np.zeros(w.B, np.int32)
+    w_out = np.zeros(1, np.int32)
+    a = np.zeros(w.B, np.int32)
+    y = np.zeros(w.B, np.int32)
+    dt = 1 if w.logit_dtype == torch.bfloat16 else 0
+    cur, total, rounds = 0, 0.0, 0
+    start = time.perf_counter()
+    while True:
+        host = lambda t: np.ascontiguousarray((t.view(torch.int16) if dt else t).numpy())  # noqa: E731
+        if w.mode == "greedy":
+            lg, d = synth.greedy_round(gen, w.B, w.D, w.V, w.alpha, dtype=w.logit_dtype)
+            raw = host(lg)
+            dd = np.ascontiguousarray(d.numpy().astype(np.int32))
+            t0 = time.perf_counter()
+            rc = lib.cpu_verify_greedy(raw.ctypes.data, dt, w.B, w.D, w.V, dd.ctypes.data,
+                                       a.ctypes.data, y.ctypes.data, threads)
+        else:
+            lg, dl, d, u = synth.sampled_round(gen, w.B, w.D, w.V, w.temperature,
+                                               dtype=w.logit_dtype)
+            raw, rawd = host(lg), host(dl)
+            dd = np.ascontiguousarray(d.numpy().astype(np.int32))
+            uu = np.ascontiguousarray(u.numpy().astype(np.float32))
+            t0 = time.perf_counter()
+            rc = lib.cpu_verify_sample(raw.ctypes.data, rawd.ctypes.data, dt, w.B, w.D, w.V,
+                                       dd.ctypes.data, uu.ctypes.data, float(w.temperature),
+                                       a.ctypes.data, y.ctypes.data, threads)
+        t1 = time.perf_counter()
+        rc |= lib.cpu_realign(kv[cur].ctypes.data, kv[1 - cur].ctypes.data, Ls, w.B, w.heads, cap,
+                              cap, w.head_dim * es, w.D, n.ctypes.data, W, a.ctypes.data,
+                              y.ctypes.data, dd.ctypes.data, ids[cur].ctypes.data,
+                              ids[1 - cur].ctypes.data, mask.ctypes.data, pos.ctypes.data,
+                              n_out.ctypes.data, w_out.ctypes.data, 0, threads)
+        t2 = time.perf_counter()
+        if rc:
+            raise RuntimeError(f"CPU baseline error {rc}")
+        n, W, cur = n_out.copy(), int(w_out[0]), 1 - cur
+        total += (t1 - t0) + (t2 - t1) * (w.layers / Ls)
+        rounds += 1
+        if time.perf_counter() - start > budget_s or rounds >= max_rounds:
+            break
+    return {"value": rounds / total, "unit": "rounds/s", "cores": threads,
+            "kind": "row-parallel C++ baseline (std::thread over score rows and K/V runs)",
+            "sample": f"{rounds} rounds: {w.mode} verification of all rows, realignment of {Ls} of "
+                      f"{w.layers} layers scaled x{w.layers / Ls:g}"}
+
+
 def run_reference(args, rank, ws):
     if rank != 0:
         return None
@@ -968,12 +1038,15 @@ def main():
             cpu = {"value": rps, "unit": "rounds/s", "cores": 1, "kind": "oracle",
                    "sample": f"{rounds} rounds: verification of all rows, realignment of {Ls} of "
                              f"{w.layers} layers scaled x{w.layers / Ls:g}"}
+        par = None
+        if ws == 1 and not args.no_cpu_baseline:
+            par = time_cpu_parallel(args.workload)
         line.update(value=res["value"], ms_per_step=res["ms_per_step"], clocks=res["clocks"],
                     e2e=res["e2e"], roofline=res["roofline"], verify=res["verify"],
                     committed_token_slots_per_s=res["committed_slots_per_s"],
                     committed_per_round=res["committed_per_round"],
                     gpu_launches=(3 if filtered else 2) * args.steps,
-                    cpu_baseline=cpu)
+                    cpu_baseline=cpu, cpu_parallel=par)
         line["config"]["cap_cols"] = res["cap_cols"]
         gb = res["bytes_per_round"] / 1e9
         line["config"]["l2"] = (
