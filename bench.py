@@ -979,9 +979,14 @@ def main():
               **({"top_k": args.top_k, "top_p": args.top_p} if filtered else {}),
               "parallelism": f"replicas x{ws}",
               "launch": args.launch}
+    # the arithmetic the path computes in: greedy verification orders the scores as they are
+    # stored (bf16 or fp32, exactly), sampled verification sums fp32 exponentials; the
+    # realignment only moves bytes
+    import torch
+    dtype = "f32" if (w.mode == "sampled" or w.logit_dtype == torch.float32) else "bf16"
     line = {"metric": METRIC, "unit": "rounds/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config}
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": config}
     if args.workload in ("exspec_pool", "exspec_serving", "exspec_sweep"):
         config["l2"] = ("inputs larger than L2: every pool round moves tens of GB of K/V; all "
                         "rounds' score rows are distinct and generated before the timed region")
