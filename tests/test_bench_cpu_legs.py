@@ -12,3 +12,31 @@ def test_parallel_leg_runs_greedy_and_sampled():
     for name in ("tiny", "glm4_9b"):
         r = bench.time_cpu_parallel(name, budget_s=0.1, max_rounds=1, layers_sample=1)
         assert r["value"] > 0 and r["cores"] >= 1 and r["unit"] == "rounds/s"
+
+
+def test_json_line_keys(monkeypatch, capsys):
+    """The bench line carries every key of its contract (the GPU leg stubbed out)."""
+    import json
+    import sys
+    fake = {"value": 10.0, "ms_per_step": 100.0, "launch": "graph+pdl",
+            "clocks": {"sm_mhz": 1, "sm_max_mhz": 1, "reasons": []},
+            "e2e": {"value": 9.0, "unit": "rounds/s", "h2d_bytes_per_step": 1,
+                    "d2h_bytes_per_step": 1},
+            "roofline": {"bound": "hbm", "achieved": 1.0, "peak": 2.0, "unit": "GB/s", "frac": 0.5,
+                         "traffic": None},
+            "verify": {}, "committed_slots_per_s": 1.0, "committed_per_round": 1.0,
+            "cap_cols": 10, "bytes_per_round": 1e10}
+    monkeypatch.setattr(bench, "run_specdec", lambda *a, **k: fake)
+    monkeypatch.setattr(bench, "dist_setup", lambda gpus: (0, 1, 0))
+    monkeypatch.setattr(bench, "time_oracle", lambda *a, **k: (2.0, 3, 1, None))
+    monkeypatch.setattr(bench, "time_cpu_parallel", lambda *a, **k: {"value": 5.0})
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", "vicuna7b"])
+    bench.main()
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "clocks",
+              "e2e", "roofline", "gpu_launches", "cpu_baseline", "cpu_parallel"):
+        assert k in line, k
+    assert line["config"]["workload"].startswith("vicuna7b")
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["gpu_launches"] == 2 * line["steps"]
