@@ -308,6 +308,20 @@ def workload(args):
     return dataclasses.replace(w, layers=args.layers) if args.layers else w
 
 
+def accept_histogram(n_hist, first, last, D):
+    """Accept lengths of rounds [first, last) from the per-round committed lengths (row r holds
+    N_b at the start of round r, so a_b = N'_b - N_b - 1): the count of each a in 0..D over all
+    rows and rounds -- a < D is also the position of the first rejected draft -- and their mean."""
+    import numpy as np
+    n = np.asarray(n_hist, dtype=np.int64)
+    a = (n[first + 1:last + 1] - n[first:last] - 1).reshape(-1)
+    if a.size and (a.min() < 0 or a.max() > D):
+        raise RuntimeError("accept length outside [0, D]")
+    hist = np.bincount(a, minlength=D + 1)[:D + 1]
+    return {"accept_len_hist": [int(x) for x in hist],
+            "mean_accept_len": float(a.mean()) if a.size else 0.0}
+
+
 def run_specdec(args, rank, ws, local):
     import numpy as np
     import torch
@@ -515,6 +529,7 @@ def run_specdec(args, rank, ws, local):
                                     verify_bytes)},
         "committed_slots_per_s": committed / (ms_max / K / 1e3),
         "committed_per_round": committed,
+        "acceptance": accept_histogram(n_hist, Wm, R, w.D),
         "cap_cols": cap,
         "bytes_per_round": realign_bytes + verify_bytes,
     }
@@ -1050,6 +1065,7 @@ def main():
                     e2e=res["e2e"], roofline=res["roofline"], verify=res["verify"],
                     committed_token_slots_per_s=res["committed_slots_per_s"],
                     committed_per_round=res["committed_per_round"],
+                    acceptance=res.get("acceptance"),
                     gpu_launches=(3 if filtered else 2) * args.steps,
                     cpu_baseline=cpu, cpu_parallel=par)
         line["config"]["cap_cols"] = res["cap_cols"]

@@ -40,3 +40,22 @@ def test_json_line_keys(monkeypatch, capsys):
     assert line["config"]["workload"].startswith("vicuna7b")
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["gpu_launches"] == 2 * line["steps"]
+
+
+def test_accept_histogram():
+    import numpy as np
+    D = 3
+    # rows' committed lengths at the start of rounds 0..3 (row r of the history)
+    n = np.array([[5, 9], [6, 13], [10, 15], [11, 16]])
+    h = bench.accept_histogram(n, 1, 3, D)     # rounds 1 and 2: a = [3, 1], [0, 0]
+    assert h["accept_len_hist"] == [2, 1, 0, 1]
+    assert h["mean_accept_len"] == 1.0
+    assert bench.accept_histogram(n, 0, 1, D)["accept_len_hist"] == [1, 0, 0, 1]
+    bad = n.copy()
+    bad[2, 0] = 20
+    try:
+        bench.accept_histogram(bad, 1, 2, D)
+    except RuntimeError:
+        pass
+    else:
+        raise AssertionError("an accept length above D must raise")
