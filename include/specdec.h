@@ -24,12 +24,14 @@
  * Conventions for every entry point:
  *   - All array arguments are DEVICE pointers owned by the caller.  The library allocates no
  *     device memory and keeps no state between calls (the host arena allocator objects, which
- *     the caller creates and destroys, are the one exception).  Greedy verification also takes a caller-owned
- *     device WORKSPACE (size from specdec_verify_greedy_workspace, 256-byte aligned) through which
- *     its CTAs exchange per-row results.  Zero-fill it once before its first use: every call
- *     leaves it all zero again (also when it reports an out-of-range input through dev_status),
- *     so it is reused as is, for any shape it is large enough for.  Calls that may overlap on the
- *     GPU need separate workspaces (one per stream).
+ *     the caller creates and destroys, and the static scratch of specdec_verify_greedy_noalloc,
+ *     are the exceptions).  Greedy verification also takes a caller-owned device WORKSPACE (size
+ *     from specdec_verify_greedy_workspace, 256-byte aligned) through which its CTAs exchange
+ *     per-row results, and the realignment and pool moves may take two caller-owned SCHEDULING
+ *     WORDS (specdec_realign_args.schedule) from which their CTAs take work items.  Zero-fill
+ *     either once before its first use: every call leaves it all zero again (also when it reports
+ *     an out-of-range input through dev_status), so it is reused as is, for any shape it is large
+ *     enough for.  Calls that may overlap on the GPU need separate ones (one per stream).
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the legacy
  *     default stream).  The return value reports host-detected problems only: an invalid
  *     argument, an unsupported configuration, or a failed launch.  It does not wait for the GPU.
