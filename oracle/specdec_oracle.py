@@ -24,7 +24,7 @@ Sources, cited by page title and section:
 * [CF]    "Correctness Forensics for Batch Speculative Decoding: Diagnosing the Ragged Tensor
           Problem", Abstract (ragged tensor problem, contiguous-layout realignment).
 
-Readings where the pages leave a step open (each is listed again in the design doc):
+Readings where the pages leave a step open (the pages are silent or ambiguous on each):
 
 * The target produces D+1 score rows per sequence; row j scores the token after the j-th draft
   (row 0 after the last committed token).  The bonus needs the distribution "after the complete
@@ -650,19 +650,21 @@ class FirstFitArena:
 # 1, 2, 3"; the uniforms u[b][j] of IE5 "Exactness Means Different Things..." drawn in-kernel]
 # --------------------------------------------------------------------------------------------
 
+# The paper's multipliers (M0, M1) and Weyl key increments (W0, W1) for each word size.
+PHILOX_CONSTANTS = {
+    32: ((0xD2511F53, 0xCD9E8D57), (0x9E3779B9, 0xBB67AE85)),
+    64: ((0xD2E7470EE14C6C93, 0xCA5A826395121157), (0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B)),
+}
+
+
 def philox(ctr, key, bits: int = 32, rounds: int = 10):
     """PhiloxNx W-R with N = 4 words of ``bits`` (32 or 64) bits: ``rounds`` rounds of
     (hi0, lo0) = M0 * c0, (hi1, lo1) = M1 * c2, c = (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0),
     the key bumped by the Weyl constants (W0, W1) between rounds."""
     mask = (1 << bits) - 1
-    if bits == 32:
-        M = (0xD2511F53, 0xCD9E8D57)
-        W = (0x9E3779B9, 0xBB67AE85)
-    elif bits == 64:
-        M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)
-        W = (0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B)
-    else:
+    if bits not in PHILOX_CONSTANTS:
         raise OracleError("word size")
+    M, W = PHILOX_CONSTANTS[bits]
     c = [int(x) & mask for x in ctr]
     k = [int(x) & mask for x in key]
     for r in range(rounds):

@@ -1,13 +1,47 @@
 """Pins of the oracle's counter-based generator (Philox, "Parallel Random Numbers: As Easy as 1,
 2, 3", SC11), used for the uniforms a fused round draws in-kernel.
 
-The 64-bit-word instance of the oracle's Philox is checked against numpy's Philox4x64-10 bit
-generator (a library routine): same round structure, multiply-high/low split and key schedule as
-the 32-bit instance the uniforms use.  Properties pin the rest."""
+The 32-bit-word instance the uniforms use is checked against the published Philox4x32-10
+known-answer vectors of the Random123 library (tests/golden/philox4x32_10_kat.json): a wrong digit
+in either multiplier or Weyl increment, or a wrong round or key schedule, changes every output
+word.  The 64-bit-word instance is checked against numpy's Philox4x64-10 bit generator (a library
+routine).  Properties pin the rest."""
+import json
+import os
+
 import numpy as np
 import pytest
 
 import oracle.specdec_oracle as O
+
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.json")
+
+
+def _kat():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("case", _kat()["cases"])
+def test_philox4x32_10_known_answers(case):
+    """The published Random123 known-answer vectors: zero counter and key, all ones, and the
+    counter and key taken from the hexadecimal digits of pi."""
+    h = lambda words: [int(w, 16) for w in words]  # noqa: E731
+    assert O.philox(h(case["ctr"]), h(case["key"]), bits=32, rounds=_kat()["rounds"]) == h(case["out"])
+
+
+@pytest.mark.parametrize("which", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_philox4x32_known_answers_catch_a_changed_constant(monkeypatch, which):
+    """Planted mistakes: one multiplier or Weyl increment with its lowest digit changed no
+    longer reproduces any of the known answers."""
+    M, W = O.PHILOX_CONSTANTS[32]
+    consts = [list(M), list(W)]
+    consts[which[0]][which[1]] ^= 0x2
+    monkeypatch.setitem(O.PHILOX_CONSTANTS, 32, (tuple(consts[0]), tuple(consts[1])))
+    h = lambda words: [int(w, 16) for w in words]  # noqa: E731
+    for case in _kat()["cases"]:
+        assert O.philox(h(case["ctr"]), h(case["key"]), bits=32) != h(case["out"])
 
 
 @pytest.mark.parametrize("ctr,key", [
