@@ -42,6 +42,14 @@
  *     spin without bound; every wait has an iteration limit (SPECDEC_ERR_TIMEOUT).
  *   - Integer outputs are bit-exact and deterministic.  Floating-point work is done in fp32 with
  *     fp64 for the few cross-block combinations stated below.
+ *   - Beyond the plainest form of each operation (its inputs, outputs, dev_status and stream),
+ *     four entry points take more, each for a stated reason: specdec_verify_greedy takes
+ *     `workspace` and `workspace_bytes` after out_token (its CTAs merge per-row results through
+ *     device memory, and the library allocates none); specdec_verify_sample takes `keep_bounds`
+ *     before dev_status (NULL: no top-k / top-p); specdec_realign_args carries `pad_id`,
+ *     `copy_engine`, `schedule` (NULL: fixed work shares) and `flags` (0, or
+ *     SPECDEC_REALIGN_PDL); specdec_realign_args and specdec_pool_args name the K/V caches by
+ *     specdec_kv_view (base pointer, element strides and sizes) rather than by a fixed layout.
  */
 #ifndef SPECDEC_H
 #define SPECDEC_H
@@ -76,6 +84,18 @@ int specdec_version(void);
 
 /* Static, human-readable name of a specdec_status value ("unknown status" otherwise). */
 const char* specdec_status_string(int status);
+
+/*
+ * Self-test of the device-side failure reporting.  The pages have no counterpart: this is a
+ * diagnostic of the library, not part of the method.  One thread of one CTA waits, with the same
+ * bounded mbarrier wait the streaming kernels use for their bulk copies, on a barrier that nothing
+ * completes: at most `polls` polls, each suspending for at most about `sleep_ns` nanoseconds.  It
+ * then writes SPECDEC_ERR_TIMEOUT to *dev_status (a device int32; the first nonzero code written
+ * stays) and exits.  No copy is issued, so nothing is in flight when it exits and the context
+ * stays usable.  Limits: 1 <= polls <= 2^20, sleep_ns <= 10^6 (so the wait ends within about a
+ * second); otherwise, or with a NULL dev_status, SPECDEC_ERR_INVALID_ARG.
+ */
+int specdec_wait_selftest(uint32_t polls, uint32_t sleep_ns, int32_t* dev_status, void* stream);
 
 /*
  * Greedy verification.  [IE5, "Exactness Means Different Things For Greedy And Sampled Output"
@@ -151,8 +171,9 @@ int specdec_verify_greedy_noalloc(const void* logits, int dtype, int B, int D, i
  *                 drafts were accepted).
  *   keep_bounds   [B][2D+1] specdec_keep_bound from specdec_sampling_filter (rows 0..D the
  *                 target's, D+1..2D the draft's), or NULL for no top-k / top-p: p_j and q_j are
- *                 then the softmax restricted to each row's kept tokens and renormalised.  A draft
- *                 outside q's kept set is accepted; outside p's only, rejected.
+ *                 then the softmax restricted to each row's kept tokens and renormalised.
+ * A draft the target cannot emit (outside p's kept set, or a score of -inf: p(d) = 0) is rejected
+ * whatever q(d) is; one with q(d) = 0 < p(d) is accepted.
  * The draw is an inverse CDF over ascending token ids: the first k whose running sum exceeds
  * u[b][D] * (total).  If max(0, p - q) is zero everywhere the draw uses p instead.
  * Precision: exponentials and per-element probabilities in fp32; the acceptance ratio p(d)/q(d)

@@ -149,7 +149,8 @@ int cpu_verify_sample(const void* target, const void* draft_scores, int dtype, i
         softmax(target, b * (D + 1) + j, p);
         softmax(draft_scores, b * D + j, q);
         const int x = draft[b * D + j];
-        const double r = q[x] > 0.0 ? p[x] / q[x] : INFINITY;
+        // q(x) = 0 < p(x) accepts; p(x) = 0 rejects whatever q(x) is
+        const double r = q[x] > 0.0 ? p[x] / q[x] : (p[x] > 0.0 ? INFINITY : 0.0);
         if (!(static_cast<double>(u[j]) < r)) {
           a = j;
           break;

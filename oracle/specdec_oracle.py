@@ -244,8 +244,8 @@ def verify_sample(target_logits, draft_logits, draft, uniforms, temperature: flo
     probability min(1, p/q).  At the first rejection j*: draw y from normalize(max(0, p_j* - q_j*)).
     If every draft is accepted: draw the bonus y from p_D.
     With top_k / top_p set, p and q are the filtered, renormalised distributions of every row
-    (filtered_softmax); a draft outside q's kept set (q(d) = 0) is accepted, one outside p's kept
-    set only is rejected.
+    (filtered_softmax); a draft the target cannot emit (p(d) = 0) is rejected whatever q(d) is,
+    and one outside q's kept set only (q(d) = 0 < p(d)) is accepted.
 
     Returns (accept_len[B], out_token[B], residual[B, V], trace) where residual[b] is the
     normalised distribution y_b was drawn from, and trace holds float64 diagnostics for the
@@ -278,7 +278,8 @@ def verify_sample(target_logits, draft_logits, draft, uniforms, temperature: flo
             p = filtered_softmax(tl[b, j], temperature, top_k, top_p)
             q = filtered_softmax(dl[b, j], temperature, top_k, top_p)
             x = int(draft[b, j])
-            r = p[x] / q[x] if q[x] > 0 else np.inf
+            # min(1, p/q): q(x) = 0 < p(x) accepts; p(x) = 0 rejects whatever q(x) is
+            r = p[x] / q[x] if q[x] > 0 else (np.inf if p[x] > 0 else 0.0)
             ratio[b, j] = r
             if not (u[b, j] < r):        # reject: stop here, later drafts are discarded
                 a = j

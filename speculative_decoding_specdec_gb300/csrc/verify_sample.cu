@@ -303,10 +303,11 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
   __shared__ float incl[kThreads];
   __shared__ float wtot[32];
   __shared__ float slice_sum[2];  // this CTA's residual total (second slot: fallback to p)
+  __shared__ int slice_fail[2];   // this CTA gave up a bounded wait (read by the whole cluster)
   __shared__ double s_R, s_P;
   __shared__ float s_tl, s_inv, s_iz, s_iw;
   __shared__ int s_owner, s_valid, s_chunk;
-  __shared__ int s_a, s_bad, s_found, s_y, s_last, s_fail;
+  __shared__ int s_a, s_bad, s_found, s_y, s_last, s_fail, s_cfail;
   __shared__ __align__(8) uint64_t full[kMaxRingStages], empty[kMaxRingStages], pbar;
   __shared__ StreamPlan plan;
   __shared__ KeepF s_keep[kMaxQ];            // the rows' keep thresholds (sampling settings)
@@ -559,11 +560,15 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
         bad = true;
         accept = false;
       } else {
-        // A draft outside a row's kept set has probability 0 there.
+        // A draft outside a row's kept set (or with score -inf) has probability 0 there.  With
+        // q(d) = 0 the draft is accepted iff p(d) > 0: a token the target cannot emit is never
+        // committed.
         const float z = masked(s_keep[lane], pre_z[lane], d);
         const float w = masked(s_keep[D + 1 + lane], pre_w[lane], d);
         if (w == kNegInf) {
-          accept = true;  // q(d) = 0
+          accept = z != kNegInf;
+        } else if (z == kNegInf) {
+          accept = false;  // p(d) = 0 < q(d)
         } else {
           // p(d)/q(d) = 2^e * S_q / S_p with e = (z - w)*c2 - (o_p - o_q).  Estimate it in fp32:
           // e as an exact float-float (TwoProd by fmaf, TwoSum), 2^e by ex2.approx of its
@@ -715,11 +720,19 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
     __syncthreads();
     return incl[kThreads - 1];
   };
-  auto exchange = [&](int slot, float Rc) {  // R over the cluster and this CTA's offset
-    if (tid == 0) slice_sum[slot] = Rc;
+  // R over the cluster and this CTA's offset; s_cfail: some CTA of the cluster gave up a wait
+  // (its partials or staged rows are incomplete), so the row's outputs are not written.
+  auto exchange = [&](int slot, float Rc) {
+    if (tid == 0) {
+      slice_sum[slot] = Rc;
+      slice_fail[slot] = s_fail;
+    }
     cluster.sync();
     if (warp == 0) {
       const float x = lane < C ? cluster.map_shared_rank(slice_sum, lane)[slot] : 0.f;
+      const int f = lane < C ? cluster.map_shared_rank(slice_fail, lane)[slot] : 0;
+      const bool any_fail = __any_sync(0xffffffffu, f != 0);
+      if (lane == 0) s_cfail = any_fail ? 1 : 0;
       ff R{0.f, 0.f}, P{0.f, 0.f};  // rank order in every CTA: P_c + Rc_c == P_{c+1} bit for bit
       for (int r = 0; r < C; ++r) {
         const float xr = __shfl_sync(0xffffffffu, x, r);
@@ -744,7 +757,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
   if (tid == 0) {  // the draw's scalar arithmetic in fp64, on one thread
     const double R = s_R, P = s_P;
     const double t = static_cast<double>(pre_u[D]) * R;
-    const bool ok = (R > 0.0) && isfinite(R) && !s_bad;
+    const bool ok = (R > 0.0) && isfinite(R) && !s_bad && !s_cfail;
     s_valid = ok ? 1 : 0;
     s_owner = (ok && Rc > 0.f && P <= t && t < P + static_cast<double>(Rc)) ? 1 : 0;
     s_tl = static_cast<float>(t - P);
@@ -816,7 +829,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
       A.out_token[b] = s_y;
     }
   }
-  if (!valid && rank == 0 && tid == 0) {
+  if (!valid && !s_cfail && rank == 0 && tid == 0) {
     set_status(A.status, SPECDEC_ERR_INPUT_RANGE);
     A.accept_len[b] = a;
     A.out_token[b] = -1;

@@ -233,8 +233,9 @@ def filtered_drafts(dl, T, top_k, top_p, seed):
     return torch.tensor(out)
 
 
-def compare_filtered(tl, dl, draft, u, T, top_k, top_p, max_excused=0.05):
-    a, y, res, st = gpu_sample(tl, dl, draft, u, T, top_k=top_k, top_p=top_p)
+def compare_filtered(tl, dl, draft, u, T, top_k, top_p, max_excused=0.05, row_stride=None):
+    a, y, res, st = gpu_sample(tl, dl, draft, u, T, row_stride=row_stride, top_k=top_k,
+                               top_p=top_p)
     assert st == 0
     tl64, dl64 = tl.double().numpy(), dl.double().numpy()
     ea, ey, eres, tr = O.verify_sample(tl64, dl64, draft.numpy(), u.double().numpy(), T,
@@ -274,15 +275,49 @@ def test_filtered_sample_matches_oracle(B, D, V, T, dtype, top_k, top_p):
     compare_filtered(tl, dl, draft, u, T, top_k, top_p)
 
 
-def test_filtered_padded_rows():
-    gen = synth.make_gen(41)
+@pytest.mark.parametrize("extra", [3, 8])
+def test_filtered_padded_rows(extra):
+    """Sampling settings on rows inside wider buffers: 3 extra elements (rows not 16-byte
+    aligned: plain loads) and 8 (aligned, strided: per-row slices), bf16 and fp32, element by
+    element against the oracle under the same tolerances as every other sampled test."""
+    gen = synth.make_gen(41 + extra)
     for dtype in (torch.bfloat16, torch.float32):
         tl, dl, _, u = synth.sampled_round(gen, 6, 3, 5000, 0.7, dtype=dtype)
-        draft = filtered_drafts(dl, 0.7, 30, 1.0, seed=6)
-        a, y, res, st = gpu_sample(tl, dl, draft, u, 0.7, row_stride=5000 + 3, top_k=30)
-        ea, ey, _, _ = O.verify_sample(tl.double().numpy(), dl.double().numpy(), draft.numpy(),
-                                       u.double().numpy(), 0.7, top_k=30)
-        assert st == 0 and (a == ea).mean() >= 0.8
+        for top_k, top_p in ((30, 1.0), (0, 0.9), (50, 0.8)):
+            draft = filtered_drafts(dl, 0.7, top_k, top_p, seed=6 + top_k)
+            compare_filtered(tl, dl, draft, u, 0.7, top_k, top_p, row_stride=5000 + extra)
+
+
+@pytest.mark.parametrize("top_k", [0, 5])
+def test_drafts_outside_the_kept_sets(top_k):
+    """Drafts the target cannot emit: outside both rows' kept sets (p(d) = q(d) = 0) and with a
+    -inf score in both rows are rejected; outside the draft row's kept set only (q(d) = 0 < p(d))
+    accepted -- as the oracle decides, element by element."""
+    gen = synth.make_gen(45 + top_k)
+    B, D, V, T = 18, 3, 1000, 0.7
+    tl, dl, draft, u = synth.sampled_round(gen, B, D, V, T, dtype=torch.float32)
+    tl64, dl64 = tl.double().numpy(), dl.double().numpy()
+    rng = np.random.default_rng(top_k)
+    for b in range(B):
+        for j in range(D):
+            case = (b + j) % 3
+            if case == 2 or top_k == 0:      # -inf in both rows: 0/0
+                d = int(rng.integers(0, V))
+                tl[b, j, d] = float("-inf")
+                dl[b, j, d] = float("-inf")
+            else:
+                kp = O.sampling_keep(tl64[b, j], T, top_k)
+                kq = O.sampling_keep(dl64[b, j], T, top_k)
+                pick = np.nonzero(~kp & ~kq)[0] if case == 0 else np.nonzero(kp & ~kq)[0]
+                if len(pick) == 0:
+                    pick = np.nonzero(~kp & ~kq)[0]
+                d = int(pick[rng.integers(0, len(pick))])
+            draft[b, j] = d
+    a, y = compare_filtered(tl, dl, draft, u, T, top_k, 1.0, max_excused=0.0)
+    ea = O.verify_sample(tl.double().numpy(), dl.double().numpy(), draft.numpy(),
+                         u.double().numpy(), T, top_k=top_k)[0]
+    np.testing.assert_array_equal(a, ea)
+    assert (a < D).any()
 
 
 def test_top_k_one_is_greedy_on_the_gpu():

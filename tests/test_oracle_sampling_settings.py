@@ -105,6 +105,30 @@ def test_filtered_sampling_preserves_the_filtered_target():
         assert abs((a == 1).mean() - pacc) < 4 * np.sqrt(pacc * (1 - pacc) / n)
 
 
+def test_drafts_outside_the_kept_sets():
+    """min(1, p/q) at the edges of the kept sets: a draft the target cannot emit (p(d) = 0) is
+    rejected for every u, also when the draft model cannot emit it either (0/0); a draft outside
+    the draft model's set only (q(d) = 0 < p(d)) is accepted for every u; the replacement after a
+    rejection is always a token the target can emit."""
+    zp = np.log(np.array([0.4, 0.3, 0.1, 0.1, 0.05, 0.05]))   # top-2 keeps {0, 1}
+    zq = np.log(np.array([0.05, 0.4, 0.3, 0.1, 0.1, 0.05]))   # top-2 keeps {1, 2}
+    tl = np.stack([zp, zp])[None]
+    dl = zq[None, None]
+    for d, want in ((4, 0), (5, 0), (2, 0), (0, 1)):
+        for u0 in (0.0, 0.3, 0.999999):
+            for u1 in (0.0, 0.5, 0.999999):
+                a, y, _, _ = O.verify_sample(tl, dl, np.array([[d]]), np.array([[u0, u1]]), 1.0,
+                                             top_k=2)
+                assert a[0] == want, (d, u0)
+                assert y[0] in (0, 1)
+    # the same 0/0 case without sampling settings: both scores -inf
+    zp2, zq2 = zp.copy(), zq.copy()
+    zp2[4] = zq2[4] = -np.inf
+    a, y, _, _ = O.verify_sample(np.stack([zp2, zp2])[None], zq2[None, None], np.array([[4]]),
+                                 np.array([[0.0, 0.5]]), 1.0)
+    assert a[0] == 0 and y[0] != 4
+
+
 def test_planted_mistakes_are_caught(monkeypatch):
     """Mistakes planted in the oracle fail the pins above: ties ordered by higher index, and the
     top-p cut taken on the mass including the token instead of the mass before it."""
