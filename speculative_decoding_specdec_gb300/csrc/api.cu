@@ -75,3 +75,30 @@ extern "C" const char* specdec_status_string(int status) {
     default: return "unknown status";
   }
 }
+
+namespace specdec {
+namespace {
+
+// One thread waits, with the bounded wait the streaming kernels use for their copies, on an
+// mbarrier that nothing arrives at (no copy is issued, so none can still be in flight when the
+// CTA exits); when the wait gives up it records SPECDEC_ERR_TIMEOUT.
+__global__ void wait_selftest_kernel(uint32_t polls, uint32_t sleep_ns, int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_sleep(&bar, 0, polls, sleep_ns)) set_status(status, SPECDEC_ERR_TIMEOUT);
+  }
+}
+
+}  // namespace
+}  // namespace specdec
+
+extern "C" int specdec_wait_selftest(uint32_t polls, uint32_t sleep_ns, int32_t* dev_status,
+                                     void* stream) {
+  if (polls < 1 || polls > (1u << 20) || sleep_ns > 1000000u || !dev_status)
+    return SPECDEC_ERR_INVALID_ARG;
+  specdec::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(polls, sleep_ns,
+                                                                                dev_status);
+  return specdec::map_cuda_error(cudaGetLastError());
+}

@@ -155,12 +155,20 @@ struct Cursor {
   }
 };
 
+// A CTA whose bounded wait ran out adds this to each ticket it takes besides its count of one,
+// so that the CTA taking the last ticket knows a contributing CTA's keys are incomplete.  The
+// count stays below it: a batch row is touched by at most 2 CTAs per SM.
+constexpr unsigned kTicketFail = 1u << 20;
+
 // After a CTA's row segments are final in s_key: merge them into the per-row keys of the
 // workspace, take one ticket per batch row touched, and decide the batch rows whose last ticket
-// this CTA took.  NT = threads of the CTA.
+// this CTA took.  `failed`: this CTA's stream gave up (SPECDEC_ERR_TIMEOUT is already set); a
+// batch row with such a contributor gets no accept length or token, but its keys and ticket are
+// still reset for the next call.  NT = threads of the CTA.
 template <int NT>
 __device__ void merge_and_decide(const GreedyArgs& A, const unsigned long long* s_key,
-                                 unsigned char* s_last, long long g0, long long g1, int nseg) {
+                                 unsigned char* s_last, long long g0, long long g1, int nseg,
+                                 bool failed) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Q = A.D + 1;
   // Merge this CTA's row segments into the per-row keys, then take one ticket per batch row.
@@ -176,7 +184,9 @@ __device__ void merge_and_decide(const GreedyArgs& A, const unsigned long long* 
     const long long r0 = b * Q * A.RU, r1 = (b + 1) * Q * A.RU - 1;  // its units
     const unsigned expected =
         static_cast<unsigned>(A.split.owner(r1) - A.split.owner(r0) + 1);
-    s_last[k] = atom_add_acq_rel_gpu(&A.ticket[b], 1u) == expected - 1u ? 1 : 0;
+    const unsigned inc = failed ? 1u + kTicketFail : 1u;
+    const unsigned old = atom_add_acq_rel_gpu(&A.ticket[b], inc);
+    s_last[k] = (old & (kTicketFail - 1u)) != expected - 1u ? 0 : (old + inc >= kTicketFail ? 2 : 1);
   }
   __syncthreads();
   for (int k = warp; k < nb; k += NT / 32) {
@@ -198,8 +208,10 @@ __device__ void merge_and_decide(const GreedyArgs& A, const unsigned long long* 
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(A.status, SPECDEC_ERR_INPUT_RANGE);
     if (lane < Q) A.key[b * Q + lane] = 0ull;  // ready for the next call
     if (lane == 0) {
-      A.accept_len[b] = a;
-      A.out_token[b] = y;
+      if (s_last[k] == 1) {  // 2: a contributing CTA's stream gave up, its keys are incomplete
+        A.accept_len[b] = a;
+        A.out_token[b] = y;
+      }
       A.ticket[b] = 0u;
     }
   }
@@ -287,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 2) greedy_kernel(const GreedyArgs A)
   flush(prow);
   __syncthreads();
 
-  merge_and_decide<kThreads>(A, s_key, s_last, g0, g1, nseg);
+  merge_and_decide<kThreads>(A, s_key, s_last, g0, g1, nseg, false);  // no waits in this kernel
 }
 
 
@@ -402,7 +414,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) greedy_ring_kernel(const Gree
   }
   __syncthreads();
   if (s_fail && tid == 0) set_status(A.status, SPECDEC_ERR_TIMEOUT);
-  merge_and_decide<kRingThreads>(A, s_key, s_last, g0, g1, nseg);
+  merge_and_decide<kRingThreads>(A, s_key, s_last, g0, g1, nseg, s_fail != 0);
 }
 
 struct Geometry {
@@ -498,23 +510,44 @@ extern "C" size_t specdec_verify_greedy_workspace(int B, int D) {
   return specdec::workspace_bytes(B, D);
 }
 
+namespace specdec {
+namespace {
+
+// The checks of greedy verification's arguments other than the workspace, in the order both
+// entry points apply them: sizes and dtype, then (for B > 0) pointers and alignment.
+int check_greedy_args(const void* logits, int dtype, int B, int D, int V, long long row_stride,
+                      const int32_t* draft, const int32_t* accept_len, const int32_t* out_token,
+                      const int32_t* dev_status) {
+  const int es = elem_size(dtype);
+  if (es == 0 || B < 0 || D < 1 || V < 1 || row_stride < V) return SPECDEC_ERR_INVALID_ARG;
+  if (D > SPECDEC_MAX_DRAFT) return SPECDEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPECDEC_OK;
+  if (!logits || !draft || !accept_len || !out_token || !dev_status) return SPECDEC_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(logits) % es != 0) return SPECDEC_ERR_INVALID_ARG;
+  return SPECDEC_OK;
+}
+
+// Scores beyond 2^40 bytes are outside this build's limits.
+bool greedy_too_large(int dtype, int B, int D, long long row_stride) {
+  return static_cast<long long>(B) * (D + 1) * row_stride * elem_size(dtype) > (1LL << 40);
+}
+
+}  // namespace
+}  // namespace specdec
+
 extern "C" int specdec_verify_greedy(const void* logits, int dtype, int B, int D, int V,
                                      long long row_stride, const int32_t* draft,
                                      int32_t* accept_len, int32_t* out_token, void* workspace,
                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
   using namespace specdec;
-  const int es = elem_size(dtype);
-  if (es == 0 || B < 0 || D < 1 || V < 1 || row_stride < V) return SPECDEC_ERR_INVALID_ARG;
-  if (D > SPECDEC_MAX_DRAFT) return SPECDEC_ERR_UNSUPPORTED;
-  if (B == 0) return SPECDEC_OK;
-  if (!logits || !draft || !accept_len || !out_token || !dev_status || !workspace)
-    return SPECDEC_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(logits) % es != 0 ||
-      reinterpret_cast<uintptr_t>(workspace) % 256 != 0 ||
+  const int rc = check_greedy_args(logits, dtype, B, D, V, row_stride, draft, accept_len,
+                                   out_token, dev_status);
+  if (rc != SPECDEC_OK || B == 0) return rc;
+  if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 ||
       workspace_bytes < specdec::workspace_bytes(B, D))
     return SPECDEC_ERR_INVALID_ARG;
-  if (static_cast<long long>(B) * (D + 1) * row_stride * es > (1LL << 40))
-    return SPECDEC_ERR_UNSUPPORTED;
+  if (greedy_too_large(dtype, B, D, row_stride)) return SPECDEC_ERR_UNSUPPORTED;
+  const int es = elem_size(dtype);
   const bool vec = reinterpret_cast<uintptr_t>(logits) % 16 == 0 && (row_stride * es) % 16 == 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SPECDEC_BF16)
@@ -563,11 +596,14 @@ extern "C" int specdec_verify_greedy_noalloc(const void* logits, int dtype, int 
                                              long long row_stride, const int32_t* draft,
                                              int32_t* accept_len, int32_t* out_token,
                                              int32_t* dev_status, void* stream) {
-  // Nothing to run, or sizes the workspace entry point rejects before it looks at a workspace.
-  if (B <= 0 || D < 1 || D > SPECDEC_MAX_DRAFT)
-    return specdec_verify_greedy(logits, dtype, B, D, V, row_stride, draft, accept_len, out_token,
-                                 nullptr, 0, dev_status, stream);
-  if (specdec::workspace_bytes(B, D) > SPECDEC_GREEDY_SCRATCH_BYTES) return SPECDEC_ERR_UNSUPPORTED;
+  // The workspace entry point's own checks first (same codes for the same mistakes), then the
+  // limit of the static scratch.
+  const int rc0 = specdec::check_greedy_args(logits, dtype, B, D, V, row_stride, draft,
+                                             accept_len, out_token, dev_status);
+  if (rc0 != SPECDEC_OK || B == 0) return rc0;
+  if (specdec::greedy_too_large(dtype, B, D, row_stride) ||
+      specdec::workspace_bytes(B, D) > SPECDEC_GREEDY_SCRATCH_BYTES)
+    return SPECDEC_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   const int rc = specdec::greedy_scratch(&scratch);
   if (rc != SPECDEC_OK) return rc;

@@ -90,6 +90,8 @@ lib.specdec_version.restype = _i
 lib.specdec_version.argtypes = []
 lib.specdec_status_string.restype = ctypes.c_char_p
 lib.specdec_status_string.argtypes = [_i]
+lib.specdec_wait_selftest.restype = _i
+lib.specdec_wait_selftest.argtypes = [ctypes.c_uint32, ctypes.c_uint32, _vp, _vp]
 _sz = ctypes.c_size_t
 lib.specdec_verify_greedy.restype = _i
 lib.specdec_verify_greedy.argtypes = [_vp, _i, _i, _i, _i, _ll, _vp, _vp, _vp, _vp, _sz, _vp, _vp]
@@ -153,6 +155,14 @@ def version() -> int:
 
 def status_string(code: int) -> str:
     return lib.specdec_status_string(int(code)).decode()
+
+
+def wait_selftest(polls, sleep_ns, status, stream=None):
+    """Run the library's bounded wait on a barrier nothing completes (at most ``polls`` polls of
+    about ``sleep_ns`` ns); it records ERR_TIMEOUT in ``status`` (int32 CUDA tensor)."""
+    _need(status, torch.int32, "status")
+    _check(lib.specdec_wait_selftest(int(polls), int(sleep_ns), _ptr(status), _stream(stream)),
+           "specdec_wait_selftest")
 
 
 def _check(rc, what):

@@ -97,7 +97,18 @@ def test_host_validation_codes():
     assert L.specdec_verify_greedy_noalloc(None, sd.BF16, 0, 4, 100, 100, None, None, None, None, None) == sd.OK
     assert L.specdec_verify_greedy_noalloc(None, sd.BF16, 1, 0, 100, 100, None, None, None, None, None) == sd.ERR_INVALID_ARG
     assert L.specdec_verify_greedy_noalloc(None, sd.BF16, 1, 32, 100, 100, None, None, None, None, None) == sd.ERR_UNSUPPORTED
-    assert L.specdec_verify_greedy_noalloc(None, sd.BF16, 4096, 5, 100, 100, None, None, None, None, None) == sd.ERR_UNSUPPORTED
+    # a shape beyond the static scratch: argument mistakes are reported as by the workspace entry
+    # point first (NULL pointers, bad dtype, row stride below V), then the scratch limit
+    assert L.specdec_verify_greedy_noalloc(None, sd.BF16, 4096, 5, 100, 100, None, None, None, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_verify_greedy_noalloc(None, 7, 4096, 5, 100, 100, None, None, None, None, None) == sd.ERR_INVALID_ARG
+    fake = 1 << 20        # stand-in device addresses: the host checks never dereference them
+    assert L.specdec_verify_greedy_noalloc(fake, sd.BF16, 4096, 5, 100, 99, fake, fake, fake, fake, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_verify_greedy_noalloc(fake + 1, sd.BF16, 4096, 5, 100, 100, fake, fake, fake, fake, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_verify_greedy_noalloc(fake, sd.BF16, 4096, 5, 100, 100, fake, fake, fake, fake, None) == sd.ERR_UNSUPPORTED
+    # the wait self-test checks its limits on the host
+    assert L.specdec_wait_selftest(0, 0, 1 << 20, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_wait_selftest(1, 0, None, None) == sd.ERR_INVALID_ARG
+    assert L.specdec_wait_selftest(1, 2000000, 1 << 20, None) == sd.ERR_INVALID_ARG
     assert L.specdec_verify_greedy_workspace(3, 32) == 0
     assert L.specdec_verify_greedy_workspace(3, 4) == 256 + 256               # keys, counters
     # realign: NULL args, empty batch, bad views

@@ -2,8 +2,9 @@
 
 specdec_verify_greedy_noalloc runs the greedy kernel on a static per-device scratch array; two
 calls in a row (different shapes, so the second reuses what the first left behind) must give
-exactly the accept lengths and tokens of specdec_verify_greedy with a fresh workspace.  The file
-is named to be collected last, so it also runs after every other test in one process.
+exactly the accept lengths and tokens of specdec_verify_greedy with a fresh workspace, and both
+those of the CPU oracle.  The file is named to be collected last, so it also runs after every
+other test in one process.
 """
 import ctypes
 
@@ -11,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle.specdec_oracle as O
 from speculative_decoding_specdec_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -44,7 +46,9 @@ def test_noalloc_matches_workspace_entry_point_two_calls():
         assert int(s0.item()) == 0 and int(s1.item()) == 0
         np.testing.assert_array_equal(a1.cpu().numpy(), a0.cpu().numpy())
         np.testing.assert_array_equal(y1.cpu().numpy(), y0.cpu().numpy())
-        assert (a1.cpu().numpy() >= 0).all()
+        ea, ey = O.verify_greedy(logits.cpu().double().numpy(), draft.cpu().numpy())
+        np.testing.assert_array_equal(a1.cpu().numpy(), ea)
+        np.testing.assert_array_equal(y1.cpu().numpy(), ey)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
