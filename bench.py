@@ -1,18 +1,24 @@
 """Benchmark of the verify + realign hot path (one step = one speculative round).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload vicuna7b|qwen3_8b|glm4_9b]
-                    [--impl specdec|reference] [--copy-engine 0|1] [--ping-pong]
+    python bench.py [--gpus N] [--steps K] [--warmup W]
+                    [--workload glm4_9b|vicuna7b|qwen3_8b|tiny|exspec_pool|exspec_serving|exspec_sweep]
+                    [--impl specdec|reference] [--ping-pong] [--no-all-configs]
 
-A step is one round: verification of the round's D drafts per row against the target's scores,
-then realignment of the left-padded batch (every layer's surviving K/V columns move to their new
-place in the one cache buffer -- rows that do not shift stay -- or, with --ping-pong, to the
-other of two buffers; ids/mask/position IDs are rebuilt).  Inputs are synthetic, seeded and resident on
-the device before the timed region; every round streams gigabytes of K/V, far more than L2.
+A step is one round: verification of the round's D drafts per row against the target's scores
+(greedy, or speculative rejection sampling for the GLM-4-9B-shaped workload), then realignment
+of the left-padded batch (every layer's surviving K/V columns move to their new place in the one
+cache buffer -- rows that do not shift stay -- or, with --ping-pong, to the other of two buffers;
+ids/mask/position IDs are rebuilt).  Inputs are synthetic, seeded and resident on the device
+before the timed region; every round streams gigabytes of K/V, far more than L2.  The default
+workload is the GLM-4-9B-shaped sampled round (the largest); the line's ``all_configs`` block
+then times every other workload the same way (tiny, Vicuna-7B- and Qwen3-8B-shaped rounds, the
+EXSPEC pool, the batch-size sweep B = 1..64), each with its own steps and ms_per_step.
 With --gpus N (under torchrun) every rank runs an independent replica of the workload (the path
 has no exchange step); ``value`` is the rounds of all ranks over the slowest rank's time.
 
---impl reference times the CPU oracle (plain numpy, float64) on this host on a bounded sample of
-the same workload; it is the deliberately slow baseline, not a target.
+--impl reference times the CPU oracle (plain numpy, float64) on this host: W untimed and K timed
+whole rounds of the same workload, one round per step; it is the deliberately slow baseline, not
+a target.
 """
 from __future__ import annotations
 
@@ -38,7 +44,7 @@ def parse():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=40)
     p.add_argument("--warmup", type=int, default=4)
-    p.add_argument("--workload", default="vicuna7b")
+    p.add_argument("--workload", default="glm4_9b")
     p.add_argument("--impl", default="specdec", choices=["specdec", "reference"])
     p.add_argument("--copy-engine", type=int, default=0)
     p.add_argument("--top-k", type=int, default=0,
@@ -63,6 +69,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--layers", type=int, default=0,
                    help="override the workload's layer count (smaller cache, e.g. for ncu)")
+    p.add_argument("--no-all-configs", action="store_true",
+                   help="time the selected workload only (no all_configs block)")
     p.add_argument("--no-cpu-baseline", action="store_true",
                    help="skip timing the oracle (cpu_baseline: null), e.g. under a profiler")
     return p.parse_args()
@@ -823,6 +831,7 @@ def run_sweep(args, rank, ws):
                 cols = cols[(wh[r + 1] - nh[r + 1]) - (wh[r] - nh[r]) != 0]
             return cols.sum()
         alg = [2.0 * moved(r) * base.token_bytes for r in range(Wm, R)]
+        committed = float(np.mean([(nh[r + 1] - nh[r]).sum() for r in range(Wm, R)]))
         padded = [2.0 * B * (wh[r + 1] - 1) * base.token_bytes for r in range(Wm, R)]
         gbs = sum(alg) / (sum(ms) / 1e3) / 1e9
         out.append({"B": B, "realign_ms_per_round": round(float(np.mean(ms)), 4),
@@ -831,6 +840,8 @@ def run_sweep(args, rank, ws):
                     "padded_copy_gb_per_round": round(float(np.mean(padded)) / 1e9, 3),
                     "mean_width": round(float(np.mean(wh[Wm + 1:R + 1])), 1),
                     "verify_ms_per_round": round(float(np.mean(vms)), 4),
+                    "round_ms": round(float(np.mean(ms)) + float(np.mean(vms)), 4),
+                    "committed_per_round": committed,
                     "verify_frac": round(vbytes / (float(np.mean(vms)) / 1e3) / 1e9 / peak, 4)})
         del eng, rounds
         torch.cuda.empty_cache()
@@ -839,28 +850,59 @@ def run_sweep(args, rank, ws):
 
 # ------------------------------------------------------------------------------ CPU oracle
 
-def oracle_round_sampler(wname, seed=0, layers_sample=2):
-    """A bounded sample of the workload for the oracle: full verification of every row, and
-    realignment of ``layers_sample`` of the layers (scaled to all layers)."""
+def host_memory_available():
+    """Bytes this process can still allocate on the host: MemAvailable, capped by the cgroup's
+    memory limit where one is set."""
+    avail = None
+    try:
+        with open("/proc/meminfo") as f:
+            for ln in f:
+                if ln.startswith("MemAvailable:"):
+                    avail = int(ln.split()[1]) * 1024
+    except OSError:
+        pass
+    try:
+        with open("/sys/fs/cgroup/memory.max") as f:
+            lim = f.read().strip()
+        with open("/sys/fs/cgroup/memory.current") as f:
+            cur = int(f.read().strip())
+        if lim != "max":
+            room = int(lim) - cur
+            avail = room if avail is None else min(avail, room)
+    except (OSError, ValueError):
+        pass
+    return avail if avail is not None else 1 << 62
+
+
+def oracle_rounds(wname, rounds, layers=None, seed=0):
+    """Full rounds of the workload for the oracle: greedy or sampled verification of every row,
+    then the realignment of the whole cache (``layers``: all of them by default), two buffers of
+    the workload's geometry and capacity for ``rounds`` rounds.  The caches are filled with a
+    constant (the oracle only moves values).  Returns (workload, layers used, one_round), where
+    one_round() generates the next round's inputs (untimed) and returns the seconds spent in the
+    oracle's verification and realignment."""
     import numpy as np
     import torch
     from oracle import specdec_oracle as O
     from speculative_decoding_specdec_gb300 import synth
 
     w = synth.WORKLOADS[wname]
+    if w.mode not in ("greedy", "sampled"):
+        raise ValueError(f"{wname}: no oracle round for this workload")
     gen = synth.make_gen(w.seed * 1000 + seed)
     n = w.prompt_lengths(gen).numpy().astype(np.int64)
+    prompts = [torch.randint(0, w.V, (int(k),), generator=gen).tolist() for k in n]
     W = int(n.max())
-    cap = w.capacity(W, rounds=64)
-    Ls = min(layers_sample, w.layers)
-    rng = np.random.default_rng(seed)
-    kv = [rng.integers(-30000, 30000, size=(Ls, 2, w.B, w.heads, cap, w.head_dim),
-                       dtype=np.int16) for _ in range(2)]
+    cap = w.capacity(W, rounds=rounds)
+    Ls = w.layers if layers is None else min(layers, w.layers)
+    dt = np.int16 if w.kv_dtype == torch.bfloat16 else np.int32  # same bytes as the K/V dtype
+    kv = [np.full((Ls, 2, w.B, w.heads, cap, w.head_dim), 7, dtype=dt) for _ in range(2)]
     ids = np.zeros((w.B, cap), np.int32)
+    for b, pr in enumerate(prompts):
+        ids[b, W - len(pr):W] = pr
     state = {"n": n, "W": W, "ids": ids, "cur": 0}
 
     def one_round():
-        """Returns (verify seconds, realign seconds); input generation is not timed."""
         if w.mode == "greedy":
             lg, d = synth.greedy_round(gen, w.B, w.D, w.V, w.alpha, dtype=w.logit_dtype)
             lg64 = lg.double().numpy()
@@ -884,10 +926,32 @@ def oracle_round_sampler(wname, seed=0, layers_sample=2):
     return w, Ls, one_round
 
 
+def oracle_bytes(wname, rounds):
+    """Host bytes the oracle's full rounds hold at once: two caches and the one a realignment
+    returns."""
+    import torch
+    from speculative_decoding_specdec_gb300 import synth
+    w = synth.WORKLOADS[wname]
+    gen = synth.make_gen(w.seed * 1000)
+    cap = w.capacity(int(w.prompt_lengths(gen).max()), rounds=rounds)
+    es = torch.tensor([], dtype=w.kv_dtype).element_size()
+    return 3 * w.layers * 2 * w.B * w.heads * cap * w.head_dim * es
+
+
+def oracle_layers(wname, rounds):
+    """None (realign every layer) when the host can hold the oracle's caches for ``rounds``
+    rounds, else the number of layers that fits (the caller scales that sample and says so)."""
+    from speculative_decoding_specdec_gb300 import synth
+    w = synth.WORKLOADS[wname]
+    need, avail = oracle_bytes(wname, rounds), host_memory_available()
+    return None if need <= 0.6 * avail else max(1, int(w.layers * 0.6 * avail / need))
+
+
 def time_oracle(wname, budget_s=15.0, max_rounds=60):
-    """Rounds/s of the oracle on a bounded sample (verify timed whole, realign on a layer sample
-    scaled to all layers)."""
-    w, Ls, one_round = oracle_round_sampler(wname)
+    """Rounds/s of the oracle over whole rounds (every layer realigned unless the host cannot
+    hold them: then a layer sample scaled to all layers), as many as fit the budget (at least
+    one).  Returns (rounds/s, rounds timed, layers realigned, workload)."""
+    w, Ls, one_round = oracle_rounds(wname, max_rounds, layers=oracle_layers(wname, max_rounds))
     total, rounds = 0.0, 0
     start = time.perf_counter()
     while True:
@@ -970,30 +1034,145 @@ def time_cpu_parallel(wname, budget_s=8.0, max_rounds=60, layers_sample=2):
 
 
 def run_reference(args, rank, ws):
+    """The reference arm: the oracle, as it stands, on this host's cores.  W untimed and then K
+    timed whole rounds of the workload (verification of every row, realignment of every layer),
+    one round per step.  Only where the host cannot hold the oracle's caches does it realign a
+    sample of the layers, scaled to all of them, and the line says so (``extrapolated``)."""
     if rank != 0:
         return None
-    rps, rounds, Ls, w = time_oracle(args.workload, budget_s=max(10.0, 2.0 * args.steps),
-                                     max_rounds=min(60, args.warmup + args.steps))
-    sample = (f"{rounds} rounds of {w.name}: verification of all {w.B} rows, realignment of "
-              f"{Ls} of {w.layers} layers scaled x{w.layers / Ls:g}")
-    return {"value": rps, "cpu_baseline": {"value": rps, "unit": "rounds/s", "cores": 1,
-                                           "kind": "oracle", "sample": sample}}
+    from speculative_decoding_specdec_gb300 import synth
+    R = args.warmup + args.steps
+    need, avail = oracle_bytes(args.workload, R), host_memory_available()
+    w, Ls, one_round = oracle_rounds(args.workload, R, layers=oracle_layers(args.workload, R))
+    for _ in range(args.warmup):
+        one_round()
+    tv, tr = 0.0, 0.0
+    for _ in range(args.steps):
+        a, b = one_round()
+        tv, tr = tv + a, tr + b
+    scale = w.layers / Ls
+    out = {"value": args.steps / (tv + tr * scale), "ms_per_step": (tv + tr) / args.steps * 1e3}
+    if Ls < w.layers:
+        out["extrapolated"] = {"layers_timed": Ls, "scale": scale,
+                               "why": f"host memory: {need / 1e9:.0f} GB needed for every layer, "
+                                      f"{avail / 1e9:.0f} GB available"}
+        sample = (f"{args.steps} rounds of {w.name} after {args.warmup} untimed: verification of "
+                  f"all {w.B} rows, realignment of {Ls} of {w.layers} layers scaled x{scale:g}")
+    else:
+        sample = (f"{args.steps} whole rounds of {w.name} after {args.warmup} untimed: "
+                  f"verification of all {w.B} rows, realignment of all {w.layers} layers")
+    out["cpu_baseline"] = {"value": out["value"], "unit": "rounds/s", "cores": 1,
+                           "kind": "oracle", "sample": sample}
+    return out
+
+
+# ------------------------------------------------------------------------------ all configs
+
+def _sub_args(args, name):
+    import argparse
+    sub = argparse.Namespace(**vars(args))
+    sub.workload, sub.no_e2e, sub.top_k, sub.top_p, sub.philox = name, True, 0, 1.0, False
+    sub.layers = 0
+    return sub
+
+
+def _release():
+    import gc
+    import torch
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def specdec_summary(name, res, K, Wm):
+    """One workload's entry of the all_configs block."""
+    from speculative_decoding_specdec_gb300 import synth
+    w = synth.WORKLOADS[name]
+    rf, vf = res["roofline"], res["verify"]
+    return {"workload": f"{w.name}: L={w.layers} KV heads={w.heads} head_dim={w.head_dim} B={w.B} "
+                        f"D={w.D} V={w.V} {w.mode} verify",
+            "steps": K, "warmup": Wm, "ms_per_step": res["ms_per_step"],
+            "rounds_per_s": res["value"],
+            "committed_token_slots_per_s": res["committed_slots_per_s"],
+            "mean_accept_len": res["acceptance"]["mean_accept_len"],
+            "realign": {"ms_per_launch": rf["ms_per_launch"], "bytes_per_launch": rf["bytes_per_launch"],
+                        "gbs": rf["achieved"], "frac": rf["frac"]},
+            "verify": {"kernel": vf["kernel"], "us_per_launch": vf["ms_per_launch"] * 1e3,
+                       "bytes_per_launch": vf["bytes_per_launch"], "gbs": vf["achieved_gbs"],
+                       "frac": vf["frac"]},
+            "launch": res["launch"], "clocks": res["clocks"]}
+
+
+def run_all_configs(args, rank, ws, headline=None):
+    """Every other workload at the same steps and warm-up, one after another on this GPU, each
+    with its own caches (freed before the next): the model-shaped EQSPEC rounds, the tiny
+    correctness-sized round, the EXSPEC pool, and the EQSPEC batch-size sweep B = 1..64."""
+    out = {}
+    if headline is not None:
+        out[args.workload] = headline
+    K, Wm = args.steps, args.warmup
+    for name in ("tiny", "vicuna7b", "qwen3_8b", "glm4_9b"):
+        if name == args.workload:
+            continue
+        _release()
+        out[name] = specdec_summary(name, run_specdec(_sub_args(args, name), rank, ws, 0), K, Wm)
+    _release()
+    pool = run_pool(_sub_args(args, "exspec_pool"), rank, ws)
+    out["exspec_pool"] = {
+        "workload": "exspec_pool: 256 sequences, L=32 KV heads=32 head_dim=128, D=5, V=32000, "
+                    "prompts from {256,...,2048}, acceptance U[0.5,0.9] per sequence, batches of "
+                    "8, greedy verify",
+        "steps": K, "warmup": Wm, "ms_per_step": pool["ms_per_step"],
+        "pool_rounds_per_s": pool["value"],
+        "gather_append": {"gbs": pool["realign_gbs"], "frac": pool["realign_frac"]},
+        "verify": {"kernel": "greedy_kernel", "us_per_launch": pool["verify"]["ms_per_launch"] * 1e3,
+                   "bytes_per_launch": pool["verify"]["bytes_per_launch"],
+                   "gbs": pool["verify"]["achieved_gbs"], "frac": pool["verify"]["frac"]},
+        "mixed_rows_per_round": round(sum(pool["mixed_rows_per_round"]) /
+                                      max(1, len(pool["mixed_rows_per_round"])), 1)}
+    _release()
+    sweep = run_sweep(_sub_args(args, "exspec_sweep"), rank, ws)
+    out["batch_sweep"] = {
+        "workload": "EQSPEC verify+realign on the contiguous layout, Vicuna-7B-shaped cache, "
+                    "prompts from {256,...,2048}, D=5, V=32000, greedy, B in 1..64, in place",
+        "steps": K, "warmup": Wm, "points": sweep["sweep"]}
+    _release()
+    return out
 
 
 # ------------------------------------------------------------------------------ main
+
+def workload_config(args, w, ws):
+    """The ``config`` both arms print: what the workload is (geometry, batch, drafts, vocabulary,
+    cache capacity, how its inputs relate to L2), nothing about how it is run."""
+    import torch
+    from speculative_decoding_specdec_gb300 import synth
+    filtered = w.mode == "sampled" and (args.top_k > 0 or args.top_p < 1.0)
+    R = args.steps + args.warmup
+    cap = w.capacity(int(w.prompt_lengths(synth.make_gen(w.seed * 1000)).max()), rounds=R)
+    les = torch.tensor([], dtype=w.logit_dtype).element_size()
+    score_bytes = w.B * (w.D + 1) * w.V * les + (w.B * w.D * w.V * les if w.mode == "sampled" else 0)
+    cache_bytes = w.token_bytes * w.B * cap
+    if score_bytes + cache_bytes > 2 * L2_BYTES:
+        l2 = (f"inputs larger than L2: a {cache_bytes / 1e9:.1f} GB K/V cache whose surviving "
+              f"columns every round moves, and {score_bytes / 1e6:.1f} MB of score rows per round, "
+              f"all rounds' rows distinct and generated before the timed region")
+    else:
+        l2 = (f"inputs smaller than L2 ({(cache_bytes + score_bytes) / 1e6:.3f} MB) and L2 not "
+              f"flushed: a latency-bound correctness-sized workload, not a bandwidth figure")
+    return {"workload": f"{w.name}: L={w.layers} KV heads={w.heads} head_dim={w.head_dim} "
+                        f"B={w.B} D={w.D} V={w.V} {w.mode} verify",
+            "B": w.B, "D": w.D, "V": w.V, "layers": w.layers, "kv_heads": w.heads,
+            "head_dim": w.head_dim, "verify": w.mode,
+            **({"top_k": args.top_k, "top_p": args.top_p} if filtered else {}),
+            "parallelism": f"replicas x{ws}", "cap_cols": cap, "l2": l2}
+
 
 def main():
     args = parse()
     rank, ws, local = dist_setup(args.gpus)
     w = workload(args)
     filtered = w.mode == "sampled" and (args.top_k > 0 or args.top_p < 1.0)  # + the filter kernel
-    config = {"workload": f"{w.name}: L={w.layers} KV heads={w.heads} head_dim={w.head_dim} "
-                          f"B={w.B} D={w.D} V={w.V} {w.mode} verify",
-              "B": w.B, "D": w.D, "V": w.V, "layers": w.layers, "kv_heads": w.heads,
-              "head_dim": w.head_dim, "verify": w.mode,
-              **({"top_k": args.top_k, "top_p": args.top_p} if filtered else {}),
-              "parallelism": f"replicas x{ws}",
-              "launch": args.launch}
     # the arithmetic the path computes in: greedy verification orders the scores as they are
     # stored (bf16 or fp32, exactly), sampled verification sums fp32 exponentials; the
     # realignment only moves bytes
@@ -1001,18 +1180,28 @@ def main():
     dtype = "f32" if (w.mode == "sampled" or w.logit_dtype == torch.float32) else "bf16"
     line = {"metric": METRIC, "unit": "rounds/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": dtype, "data": "synthetic", "config": config}
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic"}
     if args.workload in ("exspec_pool", "exspec_serving", "exspec_sweep"):
-        config["l2"] = ("inputs larger than L2: every pool round moves tens of GB of K/V; all "
-                        "rounds' score rows are distinct and generated before the timed region")
+        config = {"workload": args.workload, "parallelism": f"replicas x{ws}",
+                  "l2": "inputs larger than L2: every pool round moves tens of GB of K/V; all "
+                        "rounds' score rows are distinct and generated before the timed region"}
+    else:
+        config = workload_config(args, w, ws)
+    line["config"] = config
     if args.impl == "reference":
+        if args.workload not in ("tiny", "vicuna7b", "qwen3_8b", "glm4_9b"):
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable":
+                                  f"no oracle round for the {args.workload} workload"}))
+            return
         res = run_reference(args, rank, ws)
         if rank == 0:
-            config.pop("launch", None)   # the oracle runs on host cores: no launch mode
-            line.update(impl="reference", value=res["value"], ms_per_step=1e3 / res["value"],
+            line.update(impl="reference", value=res["value"], ms_per_step=res["ms_per_step"],
                         cpu_baseline=res["cpu_baseline"], dtype="f64",
                         e2e={"value": res["value"], "unit": "rounds/s",
                              "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0})
+            if "extrapolated" in res:
+                line["extrapolated"] = res["extrapolated"]
             print(json.dumps(line))
         return
     if args.workload == "exspec_pool":
@@ -1049,15 +1238,22 @@ def main():
             print(json.dumps(line))
         return
     cores, narrowed = bind_local_cpus(local if ws > 1 else 0)
-    config["host_cpus"] = f"{cores} cores" + (" local to the GPU (NVML affinity)" if narrowed else "")
     res = run_specdec(args, rank, ws, local)
+    every = None
+    if ws == 1 and not args.no_all_configs:
+        every = run_all_configs(args, rank, ws,
+                                headline=specdec_summary(args.workload, res, args.steps,
+                                                         args.warmup))
     if rank == 0:
         cpu = None
         if ws == 1 and not args.no_cpu_baseline:
-            rps, rounds, Ls, _ = time_oracle(args.workload, budget_s=12.0)
+            rps, rounds, Ls, _ = time_oracle(args.workload, budget_s=12.0,
+                                             max_rounds=args.steps + args.warmup)
             cpu = {"value": rps, "unit": "rounds/s", "cores": 1, "kind": "oracle",
-                   "sample": f"{rounds} rounds: verification of all rows, realignment of {Ls} of "
-                             f"{w.layers} layers scaled x{w.layers / Ls:g}"}
+                   "sample": f"{rounds} whole rounds: verification of all {w.B} rows, "
+                             f"realignment of all {w.layers} layers" if Ls == w.layers else
+                             f"{rounds} rounds: verification of all {w.B} rows, realignment of "
+                             f"{Ls} of {w.layers} layers scaled x{w.layers / Ls:g} (host memory)"}
         par = None
         if ws == 1 and not args.no_cpu_baseline:
             par = time_cpu_parallel(args.workload)
@@ -1068,19 +1264,14 @@ def main():
                     acceptance=res.get("acceptance"),
                     gpu_launches=(3 if filtered else 2) * args.steps,
                     cpu_baseline=cpu, cpu_parallel=par)
-        line["config"]["cap_cols"] = res["cap_cols"]
-        gb = res["bytes_per_round"] / 1e9
-        line["config"]["l2"] = (
-            f"inputs larger than L2: every round streams {gb:.2f} GB (K/V moved and scores "
-            f"read); all rounds' score rows are distinct and generated before the timed region"
-            if res["bytes_per_round"] > 2 * L2_BYTES else
-            f"inputs smaller than L2 ({gb * 1e3:.3f} MB per round) and L2 not flushed: a "
-            f"latency-bound correctness-sized workload, not a bandwidth figure")
-        line["config"]["launch"] = res["launch"]
-        if args.philox and w.mode == "sampled":
-            line["config"]["uniforms"] = "in-kernel Philox4x32-10"
-        line["config"]["kv_buffers"] = 2 if args.ping_pong else 1
-        line["config"]["realign_schedule"] = args.realign_schedule
+        line["run"] = {"launch": res["launch"], "kv_buffers": 2 if args.ping_pong else 1,
+                       "realign_schedule": args.realign_schedule,
+                       "host_cpus": f"{cores} cores" + (" local to the GPU (NVML affinity)"
+                                                        if narrowed else ""),
+                       **({"uniforms": "in-kernel Philox4x32-10"}
+                          if args.philox and w.mode == "sampled" else {})}
+        if every is not None:
+            line["all_configs"] = every
         print(json.dumps(line))
 
 

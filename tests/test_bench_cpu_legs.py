@@ -1,5 +1,7 @@
 """The CPU legs of bench.py (the oracle baseline and the row-parallel C++ baseline) run on tiny
 samples without a GPU, so a round-end benchmark cannot fail in them."""
+import pytest
+
 import bench
 
 
@@ -30,16 +32,44 @@ def test_json_line_keys(monkeypatch, capsys):
     monkeypatch.setattr(bench, "dist_setup", lambda gpus: (0, 1, 0))
     monkeypatch.setattr(bench, "time_oracle", lambda *a, **k: (2.0, 3, 1, None))
     monkeypatch.setattr(bench, "time_cpu_parallel", lambda *a, **k: {"value": 5.0})
+    monkeypatch.setattr(bench, "run_all_configs", lambda *a, **k: {"tiny": {}})
+    monkeypatch.setattr(bench, "specdec_summary", lambda *a, **k: {})
     monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", "vicuna7b"])
     bench.main()
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
               "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "clocks",
-              "e2e", "roofline", "gpu_launches", "cpu_baseline", "cpu_parallel"):
+              "e2e", "roofline", "gpu_launches", "cpu_baseline", "cpu_parallel", "run",
+              "all_configs"):
         assert k in line, k
     assert line["config"]["workload"].startswith("vicuna7b")
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["gpu_launches"] == 2 * line["steps"]
+    assert "launch" not in line["config"] and line["run"]["launch"] == "graph+pdl"
+
+
+def test_default_workload_is_the_sampled_glm_shape(monkeypatch):
+    import sys
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    assert bench.parse().workload == "glm4_9b"
+
+
+def test_reference_arm_times_whole_rounds_with_the_same_config(monkeypatch, capsys):
+    """--impl reference times K whole oracle rounds (every layer) after W untimed ones, reports
+    ms_per_step of those rounds, and prints the config dict the GPU arm prints."""
+    import json
+    import sys
+    monkeypatch.setattr(bench, "dist_setup", lambda gpus: (0, 1, 0))
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--workload", "tiny",
+                                      "--steps", "3", "--warmup", "1"])
+    bench.main()
+    ref = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert ref["impl"] == "reference" and ref["steps"] == 3 and ref["warmup"] == 1
+    assert ref["value"] == pytest.approx(1e3 / ref["ms_per_step"], rel=1e-9)
+    assert "extrapolated" not in ref and "all 1 layers" in ref["cpu_baseline"]["sample"]
+    assert ref["e2e"]["h2d_bytes_per_step"] == 0
+    args = bench.parse()
+    assert ref["config"] == bench.workload_config(args, bench.workload(args), 1)
 
 
 def test_accept_histogram():
