@@ -1,7 +1,8 @@
 """Benchmark of the verify + realign hot path (one step = one speculative round).
 
     python bench.py [--gpus N] [--steps K] [--warmup W]
-                    [--workload glm4_9b|vicuna7b|qwen3_8b|tiny|exspec_pool|exspec_serving|exspec_sweep]
+                    [--workload glm4_9b|vicuna7b|qwen3_8b|tiny|exspec_pool|exspec_serving|exspec_sweep|
+                                read_floor]
                     [--impl specdec|reference] [--ping-pong] [--no-all-configs]
 
 A step is one round: verification of the round's D drafts per row against the target's scores
@@ -311,7 +312,8 @@ def measured_peaks():
 def workload(args):
     import dataclasses
     from speculative_decoding_specdec_gb300 import synth
-    w = synth.WORKLOADS["exspec_pool" if args.workload in ("exspec_sweep", "exspec_serving")
+    w = synth.WORKLOADS["exspec_pool" if args.workload in ("exspec_sweep", "exspec_serving",
+                                                           "read_floor")
                         else args.workload]
     return dataclasses.replace(w, layers=args.layers) if args.layers else w
 
@@ -1066,6 +1068,98 @@ def run_reference(args, rank, ws):
     return out
 
 
+# ------------------------------------------------------------------------------ read floor
+
+def run_floor(args):
+    """How long a plain streaming read of each verification input takes on this GPU, beside the
+    verification kernel on the same bytes: CUDA events around one launch queued behind a device
+    sleep, after (a) a 2 GB device copy that leaves L2 full of dirty lines (as a realignment does
+    before the next round's verification) and (b) a 512 MB read that leaves it clean.  The plain
+    read is torch's amax over the scores (one library reduction kernel, every byte read once).
+    The inputs are the workloads' own score shapes: Vicuna-7B 3.07 MB, Qwen3-8B 24.3 MB, the
+    EXSPEC pool 98.3 MB (greedy) and GLM-4-9B 126.1 MB (sampled, target and draft rows)."""
+    import statistics
+    import torch
+    from speculative_decoding_specdec_gb300 import specdec as sd
+    from speculative_decoding_specdec_gb300 import synth
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    s = torch.cuda.current_stream()
+    clean = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    big_a = torch.empty(1 << 31, dtype=torch.uint8, device=dev)
+    big_b = torch.empty_like(big_a)
+    reps = max(5, args.steps)
+    out = []
+    for name in ("vicuna7b", "qwen3_8b", "exspec_pool", "glm4_9b"):
+        w = synth.WORKLOADS[name]
+        g = torch.Generator(device=dev).manual_seed(w.seed)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        a = torch.empty(w.B, dtype=torch.int32, device=dev)
+        y = torch.empty(w.B, dtype=torch.int32, device=dev)
+        if w.mode == "sampled":
+            tl, dl, d, u = synth.sampled_round(g, w.B, w.D, w.V, w.temperature, device=dev)
+            parts = (tl, dl)
+
+            def verify():
+                sd.verify_sample(tl, dl, d, u, w.temperature, a, y, st)
+        else:
+            lg, d = synth.greedy_round(g, w.B, w.D, w.V, 0.7, device=dev)
+            parts = (lg,)
+            ws = torch.zeros(sd.greedy_workspace_bytes(w.B, w.D), dtype=torch.uint8, device=dev)
+
+            def verify():
+                sd.verify_greedy(lg, d, a, y, st, ws)
+        nbytes = sum(x.numel() * x.element_size() for x in parts)
+        flat = torch.cat([x.reshape(-1) for x in parts])  # the same bytes in one tensor
+        red = torch.empty((), dtype=flat.dtype, device=dev)
+
+        def read():
+            torch.amax(flat, dim=0, out=red)
+        timed = [("read_us", read), ("verify_us", verify)]
+        if w.mode == "sampled":
+            # the same bytes through this library's bulk-copy streaming kernel: greedy
+            # verification of the 2D+1 rows per batch row as one score tensor
+            rows = flat.view(w.B, 2 * w.D + 1, w.V)
+            d2 = torch.randint(0, w.V, (w.B, 2 * w.D), generator=g, device=dev, dtype=torch.int32)
+            ws2 = torch.zeros(sd.greedy_workspace_bytes(w.B, 2 * w.D), dtype=torch.uint8,
+                              device=dev)
+
+            def ring_read():
+                sd.verify_greedy(rows, d2, a, y, st, ws2)
+            timed.append(("ring_read_us", ring_read))
+        row = {"workload": name, "verify": w.mode, "mb": round(nbytes / 1e6, 2)}
+        for cond in ("dirty", "clean"):
+            for what, fn in timed:
+                fn()
+                t = []
+                for _ in range(reps):
+                    if cond == "dirty":
+                        big_b.copy_(big_a)
+                    else:
+                        torch.amax(clean, dim=0)
+                    torch.cuda._sleep(100_000)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(s)
+                    fn()
+                    e1.record(s)
+                    torch.cuda.synchronize()
+                    t.append(e0.elapsed_time(e1) * 1e3)
+                row[f"{what}_{cond}"] = round(statistics.median(t), 2)
+        if int(st.item()):
+            raise RuntimeError(f"device status {int(st.item())}")
+        peak, _ = measured_peaks()
+        for cond in ("dirty", "clean"):
+            for what, _ in timed:
+                key = what[:-3]
+                row[f"{key}_frac_{cond}"] = round(
+                    nbytes / (row[f"{what}_{cond}"] * 1e-6) / 1e9 / peak, 4)
+        out.append(row)
+        del flat, parts, timed
+        torch.cuda.empty_cache()
+    return out
+
+
 # ------------------------------------------------------------------------------ all configs
 
 def _sub_args(args, name):
@@ -1181,7 +1275,7 @@ def main():
     line = {"metric": METRIC, "unit": "rounds/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": dtype, "data": "synthetic"}
-    if args.workload in ("exspec_pool", "exspec_serving", "exspec_sweep"):
+    if args.workload in ("exspec_pool", "exspec_serving", "exspec_sweep", "read_floor"):
         config = {"workload": args.workload, "parallelism": f"replicas x{ws}",
                   "l2": "inputs larger than L2: every pool round moves tens of GB of K/V; all "
                         "rounds' score rows are distinct and generated before the timed region"}
@@ -1225,6 +1319,16 @@ def main():
                                   f"greedy verify")
             line.update(value=res.pop("value"), ms_per_step=res.pop("ms_per_step"), pool=res,
                         unit="rounds/s", metric="EXSPEC serving pool rounds/s")
+            print(json.dumps(line))
+        return
+    if args.workload == "read_floor":
+        if rank == 0:
+            peak, kind = measured_peaks()
+            line.update(metric="verification launch vs plain streaming read", unit="us",
+                        value=None, higher_is_better=False, peak_gbs=peak, peak_source=kind,
+                        floor=run_floor(args))
+            line["config"] = {"workload": "read_floor: the verification inputs of vicuna7b, "
+                                          "qwen3_8b, exspec_pool and glm4_9b"}
             print(json.dumps(line))
         return
     if args.workload == "exspec_sweep":
