@@ -480,6 +480,18 @@ def run_specdec(args, rank, ws, local):
             host.append({k: v.cpu().pin_memory() for k, v in h.items()})
         feed = HostRounds(eng, host[0], stream)
         out = torch.empty((R, 3 * w.B + 1), dtype=torch.int32).pin_memory()
+        # the host link's rate for one round's inputs alone (bounds the end-to-end rate)
+        link = []
+        for rep in range(4):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            for name, t in host[rep % R].items():
+                feed.slots[0][name].copy_(t, non_blocking=True)
+            c1.record(stream)
+            torch.cuda.synchronize()
+            if rep:
+                link.append(c0.elapsed_time(c1))
+        h2d_gbs = feed.h2d_bytes / (statistics.median(link) / 1e3) / 1e9
 
         def step(d):
             if w.mode == "greedy":
@@ -512,7 +524,9 @@ def run_specdec(args, rank, ws, local):
         e2e = {"value": K * ws / (e2e_ms / 1e3), "unit": "rounds/s",
                "h2d_bytes_per_step": feed.h2d_bytes, "d2h_bytes_per_step": feed.d2h_bytes,
                "copies": "H2D on a copy stream overlapping the previous round; D2H after each "
-                         "round"}
+                         "round",
+               "h2d_gbs_alone": round(h2d_gbs, 1),
+               "copy_bound_rounds_per_s": round(h2d_gbs * 1e9 / feed.h2d_bytes, 1)}
 
     ms_max = max_over_ranks(ms, ws)
     rounds_all = sum_over_ranks(float(K), ws)
