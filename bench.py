@@ -537,6 +537,21 @@ def run_specdec(args, rank, ws, local):
     peak, peak_kind = measured_peaks()
     achieved = realign_bytes / (t_realign / 1e3) / 1e9
     verify_gbs = verify_bytes / (t_verify / 1e3) / 1e9
+    sfu = None
+    if w.mode == "sampled" and not filtered:
+        # the second roof of sampled verification: one exp2 per score of the 2D+1 rows, then two
+        # per vocabulary entry of the residual row pair (one for a bonus row), against the MUFU's
+        # nominal 16 exp2 per clock per SM at the SM clock sampled during the timed region
+        acc_hist = accept_histogram(n_hist, Wm, R, w.D)["accept_len_hist"]
+        rows_resid = sum(acc_hist[:w.D]) / K
+        rows_bonus = acc_hist[w.D] / K
+        exps = w.B * (2 * w.D + 1) * w.V + (2 * rows_resid + rows_bonus) * w.V
+        props = torch.cuda.get_device_properties(dev)
+        sm_mhz = clk.summary().get("sm_mhz") or 2070
+        mufu = 16 * props.multi_processor_count * sm_mhz * 1e6
+        sfu = {"exps_per_launch": round(exps), "exps_per_s": round(exps / (t_verify / 1e3)),
+               "peak_exps_per_s": round(mufu), "frac": round(exps / (t_verify / 1e3) / mufu, 4),
+               "peak_source": "16 exp2/clock/SM (nominal) x SMs x sampled SM clock"}
     return {
         "value": rounds_all / (ms_max / 1e3),
         "ms_per_step": ms_max / K,
@@ -554,7 +569,8 @@ def run_specdec(args, rank, ws, local):
                    "achieved_gbs": round(verify_gbs, 1), "frac": round(verify_gbs / peak, 4),
                    "traffic": None if filtered else
                    captured_traffic("greedy_kernel" if w.mode == "greedy" else "sample_kernel",
-                                    verify_bytes)},
+                                    verify_bytes),
+                   **({"sfu": sfu} if sfu else {})},
         "committed_slots_per_s": committed / (ms_max / K / 1e3),
         "committed_per_round": committed,
         "acceptance": accept_histogram(n_hist, Wm, R, w.D),
