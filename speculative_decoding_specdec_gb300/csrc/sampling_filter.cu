@@ -116,6 +116,32 @@ __device__ __forceinline__ uint32_t nraw(uint32_t key) {
   return (key & sign) ? (key & ~sign) : (~key & mask);
 }
 
+// nkey for the two bf16 scores of one 32-bit word at once (element 2i in the low half): a half
+// whose magnitude bits are zero (-0 or +0) is first made +0, then a negative half is inverted
+// and a positive one gets its top bit set.  (mag + 0x7fff) stays below 2^16 in each half, so no
+// carry crosses halves.
+__device__ __forceinline__ uint32_t nkey2(uint32_t w) {
+  const uint32_t nonzero = ((w & 0x7fff7fffu) + 0x7fff7fffu) & 0x80008000u;
+  w &= nonzero | 0x7fff7fffu;
+  const uint32_t neg = (w >> 15) & 0x00010001u;
+  return w ^ (neg * 0xffffu | 0x80008000u);
+}
+
+// How many of the two bf16 halves of w have the key of the pair pattern (pat, m) from
+// key_pattern: the halves of (w & m) ^ pat that are zero, counted by their top bit.
+__device__ __forceinline__ uint32_t count_key2(uint32_t w, uint32_t pat, uint32_t m) {
+  const uint32_t d = (w & m) ^ pat;
+  const uint32_t z = ~((((d & 0x7fff7fffu) + 0x7fff7fffu) | d)) & 0x80008000u;
+  return static_cast<uint32_t>(__popc(z));
+}
+// The raw bf16 patterns with 16-bit key `key`, for count_key2: one pattern in both halves, and a
+// mask that ignores the sign bit for the key of zero (raw +0 and -0 share it).
+__device__ __forceinline__ void key_pattern(uint32_t key, uint32_t& pat, uint32_t& m) {
+  const uint32_t raw = (key & 0x8000u) ? (key & 0x7fffu) : (~key & 0xffffu);
+  m = key == 0x8000u ? 0x7fff7fffu : 0xffffffffu;
+  pat = (raw | (raw << 16)) & m;
+}
+
 struct FilterArgs {
   const void* tl;
   const void* dl;
@@ -207,18 +233,26 @@ __device__ void pick(Shared& s, int nb, bool top_down, unsigned long long target
 // The need-th (1-based) token in index order among those with key == tkey passing `pred`:
 // every warp counts the matches of whole steps of 32*VN consecutive elements (16-byte loads,
 // four steps in flight), a prefix over the steps picks one, and warp 0 finds the token in it.
-template <typename T, typename Pred>
+template <typename T, bool kAllKept = false, typename Pred>
 __device__ __forceinline__ int nth_index(const T* x, int V, bool vec, Shared& s, uint32_t tkey,
                                          unsigned long long need, Pred pred) {
   constexpr int VN = Bits<T>::VN;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int step = 32 * VN;
   const int nst = (V + step - 1) / step;
+  // bf16 with every token eligible: compare the raw halves of each word to the key's pattern
+  uint32_t pat = 0, pm = 0;
+  if constexpr (kAllKept && Bits<T>::K == 16) key_pattern(tkey, pat, pm);
   // Matches among the lane's VN elements of step st (from its vector when the step is whole and
   // the row aligned, else element by element).
   auto count_lane = [&](int st, const uint4& r) {
     const int e0 = st * step + lane * VN;
     unsigned n = 0;
+    if constexpr (kAllKept && Bits<T>::K == 16) {
+      if (vec && e0 + VN <= V)
+        return count_key2(r.x, pat, pm) + count_key2(r.y, pat, pm) + count_key2(r.z, pat, pm) +
+               count_key2(r.w, pat, pm);
+    }
     if (vec && e0 + VN <= V) {
 #pragma unroll
       for (int i = 0; i < VN; ++i) {
@@ -241,7 +275,7 @@ __device__ __forceinline__ int nth_index(const T* x, int V, bool vec, Shared& s,
     return make_uint4(0u, 0u, 0u, 0u);
   };
   if (tid == 0) s.r_u[2] = static_cast<uint32_t>(V - 1);  // (never used: need <= matches)
-  constexpr int kSteps = 4;  // steps in flight per warp
+  constexpr int kSteps = kAllKept ? 8 : 4;  // steps in flight per warp
   for (int st0 = warp; st0 < nst; st0 += kSteps * kWarpsF) {
     uint4 r[kSteps];
 #pragma unroll
@@ -443,10 +477,33 @@ __global__ void __launch_bounds__(kFThreads, 1) filter_kernel(const FilterArgs A
       uint4* h4 = reinterpret_cast<uint4*>(hist);
       for (int i = tid; i < kHistWords / 4; i += kFThreads) h4[i] = make_uint4(0u, 0u, 0u, 0u);
       __syncthreads();
-      visit_row<T, 4>(x, V, vec, [&](int, uint32_t raw) {
-        const uint32_t key = nkey<T>(raw);
-        atomicAdd(&hist[key >> 1], 1u << ((key & 1u) << 4));
-      });
+      auto count_key = [&](uint32_t key) { atomicAdd(&hist[key >> 1], 1u << ((key & 1u) << 4)); };
+      int done_v = 0;
+      if (vec) {  // two keys per 32-bit word, five 16-byte vectors in flight per thread
+        constexpr int kFlyH = 5;
+        const uint4* v4 = reinterpret_cast<const uint4*>(x);
+        const int nv = V / 8;
+        for (int base = tid; base < nv; base += kFlyH * kFThreads) {
+          uint4 r[kFlyH];
+#pragma unroll
+          for (int k = 0; k < kFlyH; ++k)
+            if (base + k * kFThreads < nv) r[k] = v4[base + k * kFThreads];
+#pragma unroll
+          for (int k = 0; k < kFlyH; ++k) {
+            if (base + k * kFThreads < nv) {
+              const uint32_t w4[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint32_t k2 = nkey2(w4[j]);
+                count_key(k2 & 0xffffu);
+                count_key(k2 >> 16);
+              }
+            }
+          }
+        }
+        done_v = nv * 8;
+      }
+      for (int i = done_v + tid; i < V; i += kFThreads) count_key(nkey<T>(Bits<T>::raw(x + i)));
       __syncthreads();
       auto cnt = [&](uint32_t key) -> uint32_t {
         return (hist[key >> 1] >> ((key & 1u) << 4)) & 0xffffu;
@@ -475,6 +532,7 @@ __global__ void __launch_bounds__(kFThreads, 1) filter_kernel(const FilterArgs A
       {
         const uint32_t k0 = static_cast<uint32_t>(tid) * kChunk;
         const uint32_t* hw = hist + (k0 >> 1);
+#pragma unroll 8
         for (int i = 0; i < kChunk / 2; ++i) {
           const uint32_t w = static_cast<uint32_t>((i + lane) & (kChunk / 2 - 1));
           const uint32_t v = hw[w];
@@ -566,6 +624,8 @@ __global__ void __launch_bounds__(kFThreads, 1) filter_kernel(const FilterArgs A
             return c ? c * wgt(key) : 0ull;
           };
           chunk_totals([&](uint32_t w) -> unsigned long long {
+            const uint32_t v = hist[w];
+            if (v == 0u) return 0ull;  // neither value of the word occurs
             return mass_of(2 * w) + mass_of(2 * w + 1);
           });
           __syncthreads();
@@ -594,7 +654,7 @@ __global__ void __launch_bounds__(kFThreads, 1) filter_kernel(const FilterArgs A
           const unsigned long long mm = w > 0 ? (rest + w - 1) / w : 1;
           need = mm < 1 ? 1 : mm;
         }
-        const int idx = nth_index<T>(x, V, vec, s, K, need, all);
+        const int idx = nth_index<T, true>(x, V, vec, s, K, need, all);
         bound = make_uint2(score_key(Bits<T>::value(nraw<T>(K))), static_cast<uint32_t>(idx));
         if (tid == 0) A.bounds[row] = bound;
         __syncthreads();
