@@ -214,7 +214,9 @@ int specdec_philox_uniforms(uint64_t seed, uint64_t offset, int B, int D, float*
  * The kept set of one score row under the sampling settings, as its last token in the settings'
  * order.  A token with score x at index v is kept iff key(x) > key, or key(x) == key and
  * v <= index, where key(x) is the order-preserving code of the score as a float: its IEEE bits
- * with -0 taken as +0, the sign bit set for x >= 0 and all bits inverted for x < 0.
+ * with -0 taken as +0, the sign bit set for x >= 0 and all bits inverted for x < 0.  `index` is
+ * the index of the last kept token of score `key`, or INT32_MAX when every token with that score
+ * is kept (bf16 rows; fp32 rows always give the token's index).
  */
 typedef struct {
   uint32_t key;

@@ -19,8 +19,10 @@
 // atomics without return).  The highest score, the top-k cut (counts from the top) and the top-p
 // cut (count x per-value weight, from the top) then come from block scans over that histogram,
 // and one more pass (from L2) finds the index of the last kept token among the tokens of the cut
-// value.  If the counts do not add up to V (a counter passed 65535: more than 65535 equal scores)
-// the row takes the radix path instead.
+// value; that pass is skipped when the cut keeps every token of its value (the bound's index is
+// then INT_MAX).  The key code of two bf16 scores is computed in one 32-bit word, and the tie
+// search counts equal keys two per word.  If the counts do not add up to V (a counter passed
+// 65535: more than 65535 equal scores) the row takes the radix path instead.
 //
 // fp32 rows: radix selection over the order-preserving key of the score (11 + 11 + 10 bits),
 // highest level first: a shared-memory histogram per level (2048 bins at the first level, since
@@ -456,10 +458,13 @@ __global__ void __launch_bounds__(kFThreads, 1) filter_kernel(const FilterArgs A
   const bool use_k = A.top_k >= 1 && A.top_k < V;
   const bool use_p = A.top_p < 1.f;
 
-  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+  auto row_ptr = [&](long long row) -> const T* {
     const int b = static_cast<int>(row / Q), q = static_cast<int>(row % Q);
-    const T* x = q <= A.D ? static_cast<const T*>(A.tl) + (static_cast<long long>(b) * (A.D + 1) + q) * A.rs
-                          : static_cast<const T*>(A.dl) + (static_cast<long long>(b) * A.D + (q - A.D - 1)) * A.rs;
+    return q <= A.D ? static_cast<const T*>(A.tl) + (static_cast<long long>(b) * (A.D + 1) + q) * A.rs
+                    : static_cast<const T*>(A.dl) + (static_cast<long long>(b) * A.D + (q - A.D - 1)) * A.rs;
+  };
+  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+    const T* x = row_ptr(row);
     uint2 bound = make_uint2(0u, static_cast<uint32_t>(INT_MAX));  // keep all
     if (!use_k && !use_p) {
       if (tid == 0) A.bounds[row] = bound;
@@ -510,10 +515,13 @@ __global__ void __launch_bounds__(kFThreads, 1) filter_kernel(const FilterArgs A
       };
       // The 65536 keys in kFThreads chunks of kChunk, totals in s.ctot (key order).  For masses
       // (an exp2 per populated key) chunk c is summed by warp c mod kWarpsF, its lanes on
-      // consecutive words, so the few chunks that hold the row's values are spread over all warps.
+      // consecutive words, so the few chunks that hold the row's values are spread over all warps;
+      // chunks whose count is zero are skipped.
       constexpr int kChunk = 65536 / kFThreads;
       auto chunk_totals = [&](auto val_pair) {
         for (int c = warp; c < kFThreads; c += kWarpsF) {
+          // s.ctot still holds the chunk's count here: a chunk no token falls in has total 0
+          if (s.ctot[c] == 0ull) continue;
           unsigned long long t = 0;
 #pragma unroll
           for (int h = 0; h < kChunk / 64; ++h) {
@@ -654,7 +662,12 @@ __global__ void __launch_bounds__(kFThreads, 1) filter_kernel(const FilterArgs A
           const unsigned long long mm = w > 0 ? (rest + w - 1) / w : 1;
           need = mm < 1 ? 1 : mm;
         }
-        const int idx = nth_index<T, true>(x, V, vec, s, K, need, all);
+        // The tie search is needed only where the cut splits the tokens of score K: when every
+        // one of them is kept (all of K's tokens within the top-k set, where that applies), the
+        // bound's index is INT_MAX.
+        const unsigned long long eligible = (use_k && K == kk) ? krest : cnt(K);
+        const bool all_of_k = need >= eligible && (!use_k || K != kk || krest == cnt(K));
+        const int idx = all_of_k ? INT_MAX : nth_index<T, true>(x, V, vec, s, K, need, all);
         bound = make_uint2(score_key(Bits<T>::value(nraw<T>(K))), static_cast<uint32_t>(idx));
         if (tid == 0) A.bounds[row] = bound;
         __syncthreads();
