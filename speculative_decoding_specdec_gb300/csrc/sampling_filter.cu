@@ -533,21 +533,28 @@ __global__ void __launch_bounds__(kFThreads, 1) filter_kernel(const FilterArgs A
           if (lane == 0) s.ctot[c] = t;
         }
       };
-      // Counts (cheap) per thread over its own chunk, from word (lane + i) mod 64 so that the
-      // 32 lanes of a warp read 32 different banks.
+      // Counts (cheap) per thread over its own chunk, 16 bytes at a time from vector
+      // (lane + i) mod 16, so that each quarter of a warp reads 32 different banks; the highest
+      // populated key comes from the highest nonzero word.
       uint32_t km = 0;
       unsigned long long tc = 0;
       {
         const uint32_t k0 = static_cast<uint32_t>(tid) * kChunk;
         const uint32_t* hw = hist + (k0 >> 1);
-#pragma unroll 8
-        for (int i = 0; i < kChunk / 2; ++i) {
-          const uint32_t w = static_cast<uint32_t>((i + lane) & (kChunk / 2 - 1));
-          const uint32_t v = hw[w];
-          tc += (v & 0xffffu) + (v >> 16);
-          if (v >> 16) km = max(km, k0 + 2 * w + 1);
-          else if (v) km = max(km, k0 + 2 * w);
+        const uint4* hw4 = reinterpret_cast<const uint4*>(hw);
+        uint32_t lo = 0, hi = 0;
+        int wm = -1;  // highest nonzero word of the chunk
+#pragma unroll 4
+        for (int i = 0; i < kChunk / 8; ++i) {
+          const int qv = (i + lane) & (kChunk / 8 - 1);
+          const uint4 v = hw4[qv];
+          lo += (v.x & 0xffffu) + (v.y & 0xffffu) + (v.z & 0xffffu) + (v.w & 0xffffu);
+          hi += (v.x >> 16) + (v.y >> 16) + (v.z >> 16) + (v.w >> 16);
+          const int top = v.w ? 3 : v.z ? 2 : v.y ? 1 : v.x ? 0 : -1;
+          if (top >= 0) wm = max(wm, 4 * qv + top);
         }
+        tc = static_cast<unsigned long long>(lo) + hi;
+        if (wm >= 0) km = k0 + 2u * static_cast<uint32_t>(wm) + ((hw[wm] >> 16) ? 1u : 0u);
         s.ctot[tid] = tc;
       }
       // A counter that passed 65535 lost 65535 (or, carried out of its word, 65536) counts, so
