@@ -456,13 +456,30 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
                 for (int k = 0; k < 4; ++k) r[k] = v4[v + k * kConsumers];
                 float x[4][VN];
                 float m = kNegInf;
+                if constexpr (sizeof(T) == 2) {
+                  // bf16: a half is NaN iff its magnitude bits exceed 0x7f80, which one add shows
+                  // for both halves of a word (no carry crosses them); the maximum of the rest
+                  // decides the skip
+                  uint32_t nan_bits = 0;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  Vec<T>::unpack(r[k], x[k]);
+                  for (int k = 0; k < 4; ++k) {
+                    Vec<T>::unpack(r[k], x[k]);
+                    const uint32_t w4[4] = {r[k].x, r[k].y, r[k].z, r[k].w};
 #pragma unroll
-                  for (int i = 0; i < VN; ++i) m = (x[k][i] > m || x[k][i] != x[k][i]) ? x[k][i] : m;
+                    for (int j = 0; j < 4; ++j) nan_bits |= (w4[j] & 0x7fff7fffu) + 0x007f007fu;
+#pragma unroll
+                    for (int i = 0; i < VN; ++i) m = fmaxf(m, x[k][i]);
+                  }
+                  if (!(nan_bits & 0x80008000u) && m < kf.t) continue;
+                } else {
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    Vec<T>::unpack(r[k], x[k]);
+#pragma unroll
+                    for (int i = 0; i < VN; ++i) m = (x[k][i] > m || x[k][i] != x[k][i]) ? x[k][i] : m;
+                  }
+                  if (m < kf.t) continue;
                 }
-                if (m < kf.t) continue;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                   const int e0 = v0 + (v + k * kConsumers) * VN;
@@ -660,6 +677,17 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, Cfg<W>::kPerSm) sample_kerne
     float z[VN];
     Vec<T>::unpack(*reinterpret_cast<const uint4*>(zs + i), z);
     if (filter) {
+      // with sampling settings most vectors hold no kept token of row a: then every residual
+      // entry is zero (p = 0 there), and no exponential is needed (a NaN is never below the
+      // threshold, so a NaN row still goes through the arithmetic)
+      float zm = kNegInf;
+#pragma unroll
+      for (int k = 0; k < VN; ++k) zm = (z[k] > zm || z[k] != z[k]) ? z[k] : zm;
+      if (zm < kz.t) {
+#pragma unroll
+        for (int k = 0; k < VN; ++k) r[k] = 0.f;
+        return;
+      }
 #pragma unroll
       for (int k = 0; k < VN; ++k) z[k] = zmask(z[k], i + k);
     }
