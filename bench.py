@@ -1234,7 +1234,8 @@ def specdec_summary(name, res, K, Wm):
 def run_all_configs(args, rank, ws, headline=None):
     """Every other workload at the same steps and warm-up, one after another on this GPU, each
     with its own caches (freed before the next): the model-shaped EQSPEC rounds, the tiny
-    correctness-sized round, the EXSPEC pool, and the EQSPEC batch-size sweep B = 1..64."""
+    correctness-sized round, the GLM-4-9B-shaped round under top-k 50 and under top-p 0.9, the
+    EXSPEC pool, and the EQSPEC batch-size sweep B = 1..64."""
     out = {}
     if headline is not None:
         out[args.workload] = headline
@@ -1244,6 +1245,15 @@ def run_all_configs(args, rank, ws, headline=None):
             continue
         _release()
         out[name] = specdec_summary(name, run_specdec(_sub_args(args, name), rank, ws, 0), K, Wm)
+    # the sampled workload under the sampling settings (keep bounds, then masked verification)
+    for key, top_k, top_p in (("glm4_9b_top_k50", 50, 1.0), ("glm4_9b_top_p0.9", 0, 0.9)):
+        _release()
+        sub = _sub_args(args, "glm4_9b")
+        sub.top_k, sub.top_p = top_k, top_p
+        entry = specdec_summary("glm4_9b", run_specdec(sub, rank, ws, 0), K, Wm)
+        entry["workload"] += (f", top-k {top_k} (drafts from the draft model's top {top_k})"
+                              if top_k else f", top-p {top_p}")
+        out[key] = entry
     _release()
     pool = run_pool(_sub_args(args, "exspec_pool"), rank, ws)
     out["exspec_pool"] = {
