@@ -402,7 +402,7 @@ def run_specdec(args, rank, ws, local):
             if inner:
                 # a short device sleep ahead of the first event, so that on an idle GPU the
                 # events time the kernels, not the host's launch of them
-                torch.cuda._sleep(20_000)
+                torch.cuda._sleep(100_000)
                 ev[i][0].record(stream)
             verify(r)
             if inner:
@@ -481,7 +481,7 @@ def run_specdec(args, rank, ws, local):
                 if not args.philox:
                     h["uniforms"] = uniforms[r]
             host.append({k: v.cpu().pin_memory() for k, v in h.items()})
-        feed = HostRounds(eng, host[0], stream)
+        feed = HostRounds(eng, host[0], stream, timed=True)
         out = torch.empty((R, 3 * w.B + 1), dtype=torch.int32).pin_memory()
         # the host link's rate for one round's inputs alone, copied again and again from the
         # same pinned buffers (the first copy from a buffer is not timed)
@@ -520,6 +520,7 @@ def run_specdec(args, rank, ws, local):
         torch.cuda.synchronize()
         barrier(ws)
         e2e_ms = max_over_ranks(s0.elapsed_time(s1), ws)
+        copy_ms = feed.copy_ms()[-K:]  # the timed rounds' input copies
         if int(eng.status.item()):
             raise RuntimeError("device status set during the end-to-end rounds")
         n_e2e = out[:K, 2 * w.B:3 * w.B].numpy().astype(np.int64)
@@ -530,6 +531,8 @@ def run_specdec(args, rank, ws, local):
                "copies": "H2D on a copy stream overlapping the previous round; D2H after each "
                          "round",
                "h2d_gbs_repeated": round(h2d_gbs, 1),
+               "h2d_ms_per_round": {"median": round(statistics.median(copy_ms), 3),
+                                    "max": round(max(copy_ms), 3)},
                "copy_bound_rounds_per_s": round(h2d_gbs * 1e9 / feed.h2d_bytes, 1)}
 
     ms_max = max_over_ranks(ms, ws)

@@ -190,9 +190,11 @@ class HostRounds:
     third stream, so no round waits for the copy-back of the one before.
     """
 
-    def __init__(self, batch: EqspecBatch, like: dict, stream=None):
+    def __init__(self, batch: EqspecBatch, like: dict, stream=None, timed=False):
         dev = batch.status.device
         self.batch = batch
+        self.timed = timed          # record events around every input copy (copy_ms)
+        self._copy_events = []
         self.stream = stream or torch.cuda.current_stream(dev)
         self.copy_stream = torch.cuda.Stream(dev)
         self.slots = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in like.items()}
@@ -206,10 +208,21 @@ class HostRounds:
     def _stage(self, k, host, wait_freed):
         if wait_freed:
             self.copy_stream.wait_event(self.freed[k])
+        if self.timed:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(self.copy_stream)
         with torch.cuda.stream(self.copy_stream):
             for name, t in host.items():
                 self.slots[k][name].copy_(t, non_blocking=True)
         self.copied[k].record(self.copy_stream)
+        if self.timed:
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record(self.copy_stream)
+            self._copy_events.append((e0, e1))
+
+    def copy_ms(self):
+        """Milliseconds of every input copy staged so far (timed=True; synchronise first)."""
+        return [e0.elapsed_time(e1) for e0, e1 in self._copy_events]
 
     def run(self, host_rounds, step, out):
         """Run ``len(host_rounds)`` rounds.  ``host_rounds[i]`` maps input names to pinned host
