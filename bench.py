@@ -1002,10 +1002,11 @@ def time_oracle(wname, budget_s=15.0, max_rounds=60):
     return rounds / total, rounds, Ls, w
 
 
-def time_cpu_parallel(wname, budget_s=8.0, max_rounds=60, layers_sample=2):
+def time_cpu_parallel(wname, budget_s=8.0, max_rounds=60, layers_sample=None):
     """Rounds/s of the row-parallel C++ baseline (oracle/specdec_cpu_parallel.cpp, one
-    std::thread per host core) on the oracle's sample of the workload: verification of every
-    row (greedy or sampled), realignment of ``layers_sample`` layers scaled to all layers."""
+    std::thread per host core) on whole rounds of the workload: verification of every row
+    (greedy or sampled) and realignment of every layer, unless ``layers_sample`` is given or the
+    host cannot hold two caches (then that many layers, scaled to all layers, and said so)."""
     import numpy as np
     import torch
     from oracle import _build_cpu
@@ -1018,11 +1019,14 @@ def time_cpu_parallel(wname, budget_s=8.0, max_rounds=60, layers_sample=2):
     n = w.prompt_lengths(gen).numpy().astype(np.int32)
     W = int(n.max())
     cap = w.capacity(W, rounds=max_rounds)
-    Ls = min(layers_sample, w.layers)
-    rng = np.random.default_rng(0)
     es = 2 if w.kv_dtype == torch.bfloat16 else 4
-    kv = [rng.integers(-30000, 30000, size=(Ls, 2, w.B, w.heads, cap, w.head_dim * es // 2),
-                       dtype=np.int16) for _ in range(2)]
+    if layers_sample is None:  # two caches of every layer, if they fit in 60 % of free memory
+        per_layer = 2 * 2 * w.B * w.heads * cap * w.head_dim * es
+        layers_sample = max(1, min(w.layers, int(0.6 * host_memory_available() // per_layer)))
+    Ls = min(layers_sample, w.layers)
+    # K/V contents do not matter to a copy: a constant fill touches every page quickly
+    kv = [np.full((Ls, 2, w.B, w.heads, cap, w.head_dim * es // 2), 7, dtype=np.int16)
+          for _ in range(2)]
     ids = [np.zeros((w.B, cap), np.int32) for _ in range(2)]
     mask = np.zeros((w.B, cap), np.uint8)
     pos = np.zeros((w.B, cap), np.int32)
@@ -1068,8 +1072,10 @@ def time_cpu_parallel(wname, budget_s=8.0, max_rounds=60, layers_sample=2):
             break
     return {"value": rounds / total, "unit": "rounds/s", "cores": threads,
             "kind": "row-parallel C++ baseline (std::thread over score rows and K/V runs)",
-            "sample": f"{rounds} rounds: {w.mode} verification of all rows, realignment of {Ls} of "
-                      f"{w.layers} layers scaled x{w.layers / Ls:g}"}
+            "sample": f"{rounds} whole rounds: {w.mode} verification of all rows, realignment of "
+                      f"all {w.layers} layers" if Ls == w.layers else
+                      f"{rounds} rounds: {w.mode} verification of all rows, realignment of {Ls} of "
+                      f"{w.layers} layers scaled x{w.layers / Ls:g} (host memory)"}
 
 
 def run_reference(args, rank, ws):
