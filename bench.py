@@ -68,6 +68,9 @@ def parse():
                    help="realignment work distribution: CTAs take work items from a counter "
                         "(default), or every CTA moves one fixed share")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-depth", type=int, default=0,
+                   help="e2e: device staging sets for the host-fed rounds' inputs (0: as many as "
+                        "fit 1 GiB, from 2 to 8)")
     p.add_argument("--layers", type=int, default=0,
                    help="override the workload's layer count (smaller cache, e.g. for ncu)")
     p.add_argument("--no-all-configs", action="store_true",
@@ -481,7 +484,9 @@ def run_specdec(args, rank, ws, local):
                 if not args.philox:
                     h["uniforms"] = uniforms[r]
             host.append({k: v.cpu().pin_memory() for k, v in h.items()})
-        feed = HostRounds(eng, host[0], stream, timed=True)
+        round_bytes = sum(v.numel() * v.element_size() for v in host[0].values())
+        depth = args.e2e_depth or max(2, min(8, (1 << 30) // max(1, round_bytes)))
+        feed = HostRounds(eng, host[0], stream, timed=True, depth=depth)
         out = torch.empty((R, 3 * w.B + 1), dtype=torch.int32).pin_memory()
         # the host link's rate for one round's inputs alone, copied again and again from the
         # same pinned buffers (the first copy from a buffer is not timed)
@@ -528,8 +533,9 @@ def run_specdec(args, rank, ws, local):
             raise RuntimeError("end-to-end rounds committed other lengths than the device rounds")
         e2e = {"value": K * ws / (e2e_ms / 1e3), "unit": "rounds/s",
                "h2d_bytes_per_step": feed.h2d_bytes, "d2h_bytes_per_step": feed.d2h_bytes,
-               "copies": "H2D on a copy stream overlapping the previous round; D2H after each "
-                         "round",
+               "copies": "H2D on a copy stream up to staging_depth - 1 rounds ahead of the "
+                         "compute stream; D2H after each round",
+               "staging_depth": depth,
                "h2d_gbs_repeated": round(h2d_gbs, 1),
                "h2d_ms_per_round": {"median": round(statistics.median(copy_ms), 3),
                                     "max": round(max(copy_ms), 3)},

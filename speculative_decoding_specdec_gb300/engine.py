@@ -181,27 +181,32 @@ class HostRounds:
     """Rounds of one ``EqspecBatch`` fed from pinned host memory.
 
     Each round's inputs are pinned host tensors (for instance ``logits`` and ``draft``, plus
-    ``draft_logits`` and ``uniforms`` for sampled rounds).  They are copied into one of two device
-    staging sets on a copy stream while the round before runs on the compute stream, so the
-    transfer of round i + 1 overlaps the verification and realignment of round i; a staging set is
-    refilled only once the realignment that last read it has finished.  After each realignment the
+    ``draft_logits`` and ``uniforms`` for sampled rounds).  They are copied into one of ``depth``
+    device staging sets on a copy stream while earlier rounds run on the compute stream: round j
+    goes to set j mod depth, so the copy stream may run up to depth - 1 rounds ahead of the
+    verification and realignment, and a copy that the host link delays is hidden as long as that
+    lead lasts.  A staging set is refilled only once the realignment that last read it has
+    finished.  After each realignment the
     round's results (accept lengths, tokens, committed lengths and the width: 3B + 1 int32, one
     contiguous span of the batch's history) are copied into a row of a pinned host tensor on a
     third stream, so no round waits for the copy-back of the one before.
     """
 
-    def __init__(self, batch: EqspecBatch, like: dict, stream=None, timed=False):
+    def __init__(self, batch: EqspecBatch, like: dict, stream=None, timed=False, depth=2):
         dev = batch.status.device
+        if int(depth) < 1:
+            raise ValueError("depth must be at least 1")
         self.batch = batch
+        self.depth = int(depth)
         self.timed = timed          # record events around every input copy (copy_ms)
         self._copy_events = []
         self.stream = stream or torch.cuda.current_stream(dev)
         self.copy_stream = torch.cuda.Stream(dev)
         self.slots = [{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in like.items()}
-                      for _ in range(2)]
+                      for _ in range(self.depth)]
         self.d2h_stream = torch.cuda.Stream(dev)
-        self.copied = [torch.cuda.Event() for _ in range(2)]
-        self.freed = [torch.cuda.Event() for _ in range(2)]
+        self.copied = [torch.cuda.Event() for _ in range(self.depth)]
+        self.freed = [torch.cuda.Event() for _ in range(self.depth)]
         self.h2d_bytes = sum(v.numel() * v.element_size() for v in like.values())
         self.d2h_bytes = (3 * batch.B + 1) * 4
 
@@ -237,14 +242,17 @@ class HostRounds:
         if (out.dtype != torch.int32 or out.dim() != 2 or out.shape[0] < n
                 or out.shape[1] != 3 * B + 1 or not out.is_pinned()):
             raise ValueError("out must be a pinned int32 tensor [rounds, 3B + 1]")
+        P = self.depth
         start = torch.cuda.Event()
         start.record(self.stream)
         self.copy_stream.wait_event(start)   # no copy starts before the work issued so far
-        self._stage(0, host_rounds[0], False)
+        for j in range(min(P - 1, n)):       # fill: every set but one, nothing to wait for
+            self._stage(j, host_rounds[j], False)
         for i in range(n):
-            if i + 1 < n:
-                self._stage((i + 1) % 2, host_rounds[i + 1], i >= 1)
-            k = i % 2
+            j = i + P - 1                    # its set was last read by round i - 1
+            if j < n:
+                self._stage(j % P, host_rounds[j], i >= 1)
+            k = i % P
             self.stream.wait_event(self.copied[k])
             inp = self.slots[k]
             with torch.cuda.stream(self.stream):

@@ -25,9 +25,11 @@ def _batch(B, D, V, rounds, seed, in_place, L=2, H=2, hd=64):
     return gen, eng, prompts, W
 
 
-@pytest.mark.parametrize("in_place", [True, False])
+@pytest.mark.parametrize("in_place,depth", [(True, 2), (False, 2), (True, 1), (True, 4),
+                                            (False, 8)])
 @pytest.mark.parametrize("B,D,V", [(3, 4, 1000), (8, 5, 4099)])
-def test_greedy_host_rounds_match_oracle(B, D, V, in_place):
+def test_greedy_host_rounds_match_oracle(B, D, V, in_place, depth):
+    """Staging depths 1 (no overlap), 2, 4 and 8 (more sets than rounds) commit the same."""
     from speculative_decoding_specdec_gb300.engine import HostRounds
     rounds = 6
     gen, eng, prompts, W = _batch(B, D, V, rounds, 11 + B, in_place)
@@ -35,7 +37,7 @@ def test_greedy_host_rounds_match_oracle(B, D, V, in_place):
     for _ in range(rounds):
         lg, d = synth.greedy_round(gen, B, D, V, 0.7, dtype=torch.float32)
         host.append({"logits": lg.pin_memory(), "draft": d.pin_memory()})
-    feed = HostRounds(eng, host[0])
+    feed = HostRounds(eng, host[0], depth=depth)
     assert feed.h2d_bytes == B * (D + 1) * V * 4 + B * D * 4
     out = torch.zeros((rounds, 3 * B + 1), dtype=torch.int32).pin_memory()
     src0 = host_bits(eng.cache)
@@ -81,15 +83,16 @@ def test_sampled_host_rounds_match_device_rounds():
         eng.realign(dv["draft"])
         want.append(torch.cat([eng.accept_len, eng.out_token, eng.n_committed,
                                eng.width]).cpu())
-    eng.start(prompts)
-    feed = HostRounds(eng, host[0])
-    out = torch.zeros((rounds, 3 * B + 1), dtype=torch.int32).pin_memory()
-    feed.run(host, lambda d: eng.verify_sample(d["logits"], d["draft_logits"], d["draft"],
-                                               d["uniforms"], T), out)
-    torch.cuda.synchronize()
-    assert int(eng.status.item()) == 0
-    for r in range(rounds):
-        assert out[r].tolist() == want[r].tolist()
+    for depth in (2, 3):
+        eng.start(prompts)
+        feed = HostRounds(eng, host[0], depth=depth)
+        out = torch.zeros((rounds, 3 * B + 1), dtype=torch.int32).pin_memory()
+        feed.run(host, lambda d: eng.verify_sample(d["logits"], d["draft_logits"], d["draft"],
+                                                   d["uniforms"], T), out)
+        torch.cuda.synchronize()
+        assert int(eng.status.item()) == 0
+        for r in range(rounds):
+            assert out[r].tolist() == want[r].tolist()
 
 
 def test_host_rounds_rejects_unpinned_output():
