@@ -401,6 +401,56 @@ def test_keep_bounds_many_equal_scores(ties, top_k, top_p):
         assert 0 < got.sum() < ties
 
 
+@pytest.mark.parametrize("V,top_k,top_p,plant", [
+    (20480, 128, 1.0, None),
+    (20483, 7, 1.0, None),                 # ragged rows: aligned and unaligned rows in one CTA
+    (32000, 100, 1.0, ((300, 8.0),)),      # the cut inside 300 equal top scores
+    (32000, 100, 1.0, ((700, 8.0),)),
+    (32000, 100, 1.0, ((5000, 8.0),)),
+    (32000, 100, 1.0, ((60, 9.0), (200, 8.0))),   # the cut inside the second score value
+    (32000, 10, 1.0, "constant"),          # every score equal
+    (32000, 120, 0.5, ((300, 8.0),)),      # top-k then top-p, the cut inside equal scores
+    (151552, 128, 0.9, None),              # top-p inside the top 128
+    (151552, 1, 1.0, None),
+])
+def test_keep_bounds_ties_at_the_cut(V, top_k, top_p, plant):
+    """Top-k (and top-k then top-p) cuts that fall inside a run of equal scores, so the bound's
+    index comes from the tie search: kept sets equal the oracle's, with exactly k tokens kept,
+    also on ragged rows and on a row of equal scores."""
+    import speculative_decoding_specdec_gb300.specdec as sd
+    B, D = 3, 2
+    gen = synth.make_gen(900 + V + top_k)
+    tl, dl, _, _ = synth.sampled_round(gen, B, D, V, 0.7, dtype=torch.bfloat16)
+    g = torch.Generator().manual_seed(V + top_k)
+    for rows3 in (tl, dl):
+        for b in range(B):
+            for j in range(rows3.shape[1]):
+                if plant == "constant":
+                    rows3[b, j] = 0.25
+                elif plant:
+                    idx = torch.randperm(V, generator=g)
+                    at = 0
+                    for n, val in plant:
+                        rows3[b, j, idx[at:at + n]] = val
+                        at += n
+    bounds = torch.zeros((B, 2 * D + 1, 2), dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sd.sampling_filter(tl.to(DEV), dl.to(DEV), 0.7, top_k, top_p, bounds, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    bnd = bounds.cpu().numpy().astype(np.int64)
+    rows = rows_of(tl.float().numpy(), dl.float().numpy())
+    for b in range(B):
+        for q in range(2 * D + 1):
+            got = kept_from_bounds(rows[b, q], bnd[b, q])
+            exp = O.sampling_keep(rows[b, q].astype(np.float64), 0.7, top_k, top_p)
+            if not np.array_equal(got, exp):
+                assert top_p < 1.0, (b, q)
+                assert O.top_p_margin(rows[b, q].astype(np.float64), 0.7, top_k, top_p) < 2e-6
+            if top_p == 1.0:
+                assert got.sum() == top_k
+
+
 @pytest.mark.parametrize("seed,offset,B,D", [
     (0, 0, 3, 4),
     (2024, 7, 64, 6),
