@@ -484,15 +484,23 @@ __global__ void __launch_bounds__(kFThreads, 1) filter_kernel(const FilterArgs A
       __syncthreads();
       auto count_key = [&](uint32_t key) { atomicAdd(&hist[key >> 1], 1u << ((key & 1u) << 4)); };
       int done_v = 0;
-      if (vec) {  // two keys per 32-bit word, five 16-byte vectors in flight per thread
+      if (vec) {  // two keys per 32-bit word; five 16-byte vectors per batch per thread, the next
+                  // batch's loads issued before this batch is counted
         constexpr int kFlyH = 5;
         const uint4* v4 = reinterpret_cast<const uint4*>(x);
         const int nv = V / 8;
+        uint4 nx[kFlyH];
+#pragma unroll
+        for (int k = 0; k < kFlyH; ++k)
+          if (tid + k * kFThreads < nv) nx[k] = v4[tid + k * kFThreads];
         for (int base = tid; base < nv; base += kFlyH * kFThreads) {
           uint4 r[kFlyH];
 #pragma unroll
+          for (int k = 0; k < kFlyH; ++k) r[k] = nx[k];
+          const int nb = base + kFlyH * kFThreads;
+#pragma unroll
           for (int k = 0; k < kFlyH; ++k)
-            if (base + k * kFThreads < nv) r[k] = v4[base + k * kFThreads];
+            if (nb + k * kFThreads < nv) nx[k] = v4[nb + k * kFThreads];
 #pragma unroll
           for (int k = 0; k < kFlyH; ++k) {
             if (base + k * kFThreads < nv) {
