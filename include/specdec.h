@@ -68,7 +68,7 @@ extern "C" {
 typedef enum {
   SPECDEC_OK = 0,
   SPECDEC_ERR_INVALID_ARG = 1, /* host: NULL pointer, negative or inconsistent size, aliasing */
-  SPECDEC_ERR_UNSUPPORTED = 2, /* host: valid but outside this build's limits (sizes, alignment) */
+  SPECDEC_ERR_UNSUPPORTED = 2, /* host: valid but outside the library's limits (sizes, alignment) */
   SPECDEC_ERR_CUDA = 3,        /* host: a CUDA launch or attribute call failed */
   SPECDEC_ERR_CAPACITY = 4,    /* device: the new width (+ D columns for the next pass) does not
                                   fit the destination; nothing was moved */

@@ -527,7 +527,7 @@ int check_greedy_args(const void* logits, int dtype, int B, int D, int V, long l
   return SPECDEC_OK;
 }
 
-// Scores beyond 2^40 bytes are outside this build's limits.
+// Scores beyond 2^40 bytes are outside the library's limits.
 bool greedy_too_large(int dtype, int B, int D, long long row_stride) {
   return static_cast<long long>(B) * (D + 1) * row_stride * elem_size(dtype) > (1LL << 40);
 }
