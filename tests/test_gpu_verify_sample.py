@@ -116,6 +116,22 @@ def test_low_acceptance_sharp_temperature():
     compare(tl, dl, draft, u, 0.25)
 
 
+@pytest.mark.parametrize("T,scale,dtype", [
+    (0.05, 1.0, torch.bfloat16),    # nearly greedy: most exponents underflow
+    (4.0, 1.0, torch.bfloat16),     # nearly flat
+    (1.0, 12.0, torch.bfloat16),    # scores spread like a real model's (tens of units)
+    (0.05, 1.0, torch.float32),
+    (1.0, 30.0, torch.float32),
+])
+def test_sample_extreme_temperature_and_scale(T, scale, dtype):
+    """Sharp and flat temperatures and widely spread scores, under the same tolerances."""
+    gen = synth.make_gen(50 + int(T * 100) + int(scale))
+    tl, dl, draft, u = synth.sampled_round(gen, 8, 4, 32000, T, dtype=dtype)
+    tl = (tl.float() * scale).to(dtype)
+    dl = (dl.float() * scale).to(dtype)
+    compare(tl, dl, draft, u, T)
+
+
 def test_emitted_token_follows_p_chi_square():
     """Distribution preservation on the GPU: with drafts drawn from q, the first emitted token of
     many independent rows is distributed as p."""
@@ -218,6 +234,35 @@ def test_keep_bounds_match_the_oracle(B, D, V, dtype, top_k, top_p):
                 assert O.top_p_margin(rows[b, q].astype(np.float64), 0.7, top_k, top_p) < 2e-6, (b, q)
                 excused += 1
     assert excused <= max(1, 0.02 * B * (2 * D + 1))
+
+
+@pytest.mark.parametrize("T,scale,top_k,top_p", [
+    (0.05, 1.0, 0, 0.9),       # nearly all mass on the highest score or two
+    (4.0, 12.0, 0, 0.9),       # widely spread scores at a flat temperature
+    (0.05, 12.0, 40, 0.95),
+    (4.0, 1.0, 100, 0.5),
+])
+def test_keep_bounds_extreme_temperature_and_scale(T, scale, top_k, top_p):
+    """Keep bounds at sharp and flat temperatures and on widely spread bf16 scores."""
+    import speculative_decoding_specdec_gb300.specdec as sd
+    B, D, V = 4, 3, 32000
+    gen = synth.make_gen(60 + top_k + int(scale))
+    tl, dl, _, _ = synth.sampled_round(gen, B, D, V, T, dtype=torch.bfloat16)
+    tl = (tl.float() * scale).to(torch.bfloat16)
+    dl = (dl.float() * scale).to(torch.bfloat16)
+    bounds = torch.zeros((B, 2 * D + 1, 2), dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sd.sampling_filter(tl.to(DEV), dl.to(DEV), T, top_k, top_p, bounds, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    bnd = bounds.cpu().numpy().astype(np.int64)
+    rows = rows_of(tl.float().numpy(), dl.float().numpy())
+    for b in range(B):
+        for q in range(2 * D + 1):
+            got = kept_from_bounds(rows[b, q], bnd[b, q])
+            exp = O.sampling_keep(rows[b, q].astype(np.float64), T, top_k, top_p)
+            if not np.array_equal(got, exp):
+                assert O.top_p_margin(rows[b, q].astype(np.float64), T, top_k, top_p) < 2e-6, (b, q)
 
 
 def filtered_drafts(dl, T, top_k, top_p, seed):
