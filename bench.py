@@ -1124,7 +1124,9 @@ def run_floor(args):
     verification kernel on the same bytes: CUDA events around one launch queued behind a device
     sleep, after (a) a 2 GB device copy that leaves L2 full of dirty lines (as a realignment does
     before the next round's verification) and (b) a 512 MB read that leaves it clean.  The plain
-    read is torch's amax over the scores (one library reduction kernel, every byte read once).
+    reads are torch's amax over the bf16 scores and torch's sum over the same bytes viewed as
+    fp32 (its fastest plain read here: 6.4 TB/s over 4 GB); each is one library reduction kernel
+    that reads every byte once.
     The inputs are the workloads' own score shapes: Vicuna-7B 3.07 MB, Qwen3-8B 24.3 MB, the
     EXSPEC pool 98.3 MB (greedy) and GLM-4-9B 126.1 MB (sampled, target and draft rows)."""
     import statistics
@@ -1162,9 +1164,15 @@ def run_floor(args):
         flat = torch.cat([x.reshape(-1) for x in parts])  # the same bytes in one tensor
         red = torch.empty((), dtype=flat.dtype, device=dev)
 
+        words = flat.view(torch.float32)  # the same bytes as fp32 words
+        red32 = torch.empty((), dtype=torch.float32, device=dev)
+
         def read():
             torch.amax(flat, dim=0, out=red)
-        timed = [("read_us", read), ("verify_us", verify)]
+
+        def sum_read():
+            torch.sum(words, dim=0, out=red32)
+        timed = [("read_us", read), ("sum_read_us", sum_read), ("verify_us", verify)]
         if w.mode == "sampled":
             # the same bytes through this library's bulk-copy streaming kernel: greedy
             # verification of the 2D+1 rows per batch row as one score tensor
